@@ -1,0 +1,193 @@
+"""TEST INFRASTRUCTURE — fp64 CPU oracle for the batched dense product.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline / reference
+legs of ``bench.py`` may import this package.  The GPU library never does, and
+this package imports nothing from the GPU library: the two share no code.
+
+The arithmetic lives in ``bmm_oracle.c`` (plain C, fp64, k-ascending sums);
+this module only compiles it with gcc and marshals numpy arrays through
+ctypes.  What it computes is the plain definition
+
+    C_ref[b,i,j] = alpha * sum_k opA[b,i,k] * opB[b,k,j] + beta * C_in[b,i,j]
+    Bnd[b,i,j]   = sum_k |opA[b,i,k]| * |opB[b,k,j]|
+
+which the tiled kernels of "Triton Optimization Reference (cuTile -> Triton)"
+sections 1-2 (EVEN_K fast path, transpose in the addressing) reorganise but do
+not change.  Inputs are raw 16-bit patterns (``numpy.uint16``) as produced by
+the seeded input generator; C_in is ``float32`` values or bf16 bit patterns.
+
+Every function here is pinned by ``tests/test_oracle_pins.py`` against closed
+forms, brute force, exact small-integer cases and a float64 library matmul.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "bmm_oracle.c")
+_LIBDIR = os.path.join(_HERE, "_lib")
+_LIB = os.path.join(_LIBDIR, "liboracle_bmm.so")
+
+BF16, F16, F32 = 0, 1, 2
+_TYPE_CODES = {"bf16": BF16, "f16": F16, "f32": F32}
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (portable flags only) and return the path."""
+    os.makedirs(_LIBDIR, exist_ok=True)
+    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
+        return _LIB
+    tmp = _LIB + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm", "-lpthread"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def build_command() -> list:
+    """The gcc command line ``build()`` runs (for parallel builds)."""
+    return ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-o", _LIB, _SRC, "-lm", "-lpthread"]
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    build()
+    lib = ctypes.CDLL(_LIB)
+    i64, i32, f64 = ctypes.c_int64, ctypes.c_int, ctypes.c_double
+    vp = ctypes.c_void_p
+    lib.oracle_bmm_f64.argtypes = [i64] * 10 + [i32] * 4 + [f64, f64] + [vp] * 5 + [i32]
+    lib.oracle_bmm_f64.restype = i32
+    lib.oracle_bmm_sampled.argtypes = [i64] * 10 + [i32] * 4 + [f64, f64] + [vp] * 3 + [i64] + [vp] * 5
+    lib.oracle_bmm_sampled.restype = i32
+    lib.oracle_attention_probs_bf16.argtypes = [i64, i64, i64, f64, vp, vp, vp, i32]
+    lib.oracle_attention_probs_bf16.restype = i32
+    lib.oracle_round_bf16.argtypes = [f64]
+    lib.oracle_round_bf16.restype = ctypes.c_uint16
+    lib.oracle_decode16.argtypes = [ctypes.c_uint16, i32]
+    lib.oracle_decode16.restype = f64
+    _lib = lib
+    return lib
+
+
+def host_threads() -> int:
+    """Threads the oracle uses by default: every core in this process's mask."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover - non-Linux
+        return os.cpu_count() or 1
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _bits(a, name):
+    a = np.ascontiguousarray(a)
+    if a.dtype != np.uint16:
+        raise TypeError(f"{name} must hold raw 16-bit patterns (numpy.uint16), got {a.dtype}")
+    return a
+
+
+def _cin(c, typeC):
+    if c is None:
+        return None
+    c = np.ascontiguousarray(c)
+    want = np.float32 if typeC == F32 else np.uint16
+    if c.dtype != want:
+        raise TypeError(f"C_in must be {np.dtype(want).name} for this output type, got {c.dtype}")
+    return c
+
+
+def bmm(A, B, C_in, *, batch, M, N, K, lda, ldb, ldc, sA, sB, sC,
+        transA=False, transB=False, type_ab="bf16", type_c="f32",
+        alpha=1.0, beta=0.0, threads=None, want_bound=True):
+    """Full oracle.  Returns ``(C_ref, Bnd)`` as dense float64 [batch, M, N]
+    arrays (``Bnd`` is None when ``want_bound`` is false)."""
+    lib = _load()
+    ta, tc = _TYPE_CODES[type_ab], _TYPE_CODES[type_c]
+    A, B = _bits(A, "A"), _bits(B, "B")
+    C_in = _cin(C_in, tc) if beta != 0.0 else None
+    cref = np.empty((batch, M, N), dtype=np.float64)
+    bnd = np.empty((batch, M, N), dtype=np.float64) if want_bound else None
+    rc = lib.oracle_bmm_f64(batch, M, N, K, lda, ldb, ldc, sA, sB, sC,
+                            int(bool(transA)), int(bool(transB)), ta, tc,
+                            float(alpha), float(beta), _ptr(A), _ptr(B), _ptr(C_in),
+                            _ptr(cref), _ptr(bnd), int(threads or host_threads()))
+    if rc != 0:
+        raise ValueError(f"oracle_bmm_f64 rejected the problem (code {rc})")
+    return cref, bnd
+
+
+def bmm_sampled(A, B, C_in, samples, *, batch, M, N, K, lda, ldb, ldc, sA, sB, sC,
+                transA=False, transB=False, type_ab="bf16", type_c="f32",
+                alpha=1.0, beta=0.0):
+    """Oracle for chosen output elements.  ``samples`` is an int64 array of
+    shape [n, 3] holding (b, i, j).  Returns ``(c_ref, bnd)`` float64 [n]."""
+    lib = _load()
+    ta, tc = _TYPE_CODES[type_ab], _TYPE_CODES[type_c]
+    A, B = _bits(A, "A"), _bits(B, "B")
+    C_in = _cin(C_in, tc) if beta != 0.0 else None
+    s = np.ascontiguousarray(np.asarray(samples, dtype=np.int64).reshape(-1, 3))
+    ib, ii, ij = (np.ascontiguousarray(s[:, c]) for c in range(3))
+    n = s.shape[0]
+    cref = np.empty(n, dtype=np.float64)
+    bnd = np.empty(n, dtype=np.float64)
+    rc = lib.oracle_bmm_sampled(batch, M, N, K, lda, ldb, ldc, sA, sB, sC,
+                                int(bool(transA)), int(bool(transB)), ta, tc,
+                                float(alpha), float(beta), _ptr(A), _ptr(B), _ptr(C_in),
+                                n, _ptr(ib), _ptr(ii), _ptr(ij), _ptr(cref), _ptr(bnd))
+    if rc != 0:
+        raise ValueError(f"oracle_bmm_sampled rejected the problem (code {rc})")
+    return cref, bnd
+
+
+def attention_probs_bf16(Q, Kmat, *, batch, L, D, alpha, threads=None):
+    """P = bf16(row-softmax(alpha * Q K^T)) from dense [batch, L, D] bf16 bit
+    arrays, computed in fp64 and rounded once.  Returns uint16 [batch, L, L]."""
+    lib = _load()
+    Q, Kmat = _bits(Q, "Q"), _bits(Kmat, "K")
+    P = np.empty((batch, L, L), dtype=np.uint16)
+    rc = lib.oracle_attention_probs_bf16(batch, L, D, float(alpha), _ptr(Q), _ptr(Kmat),
+                                         _ptr(P), int(threads or host_threads()))
+    if rc != 0:
+        raise ValueError(f"oracle_attention_probs_bf16 failed (code {rc})")
+    return P
+
+
+def round_bf16(x):
+    """Round float64 values to bf16 (ties to even); returns uint16 bits."""
+    lib = _load()
+    x = np.asarray(x, dtype=np.float64)
+    out = np.fromiter((lib.oracle_round_bf16(float(v)) for v in x.ravel()),
+                      dtype=np.uint16, count=x.size)
+    return out.reshape(x.shape)
+
+
+def decode(bits, type_ab):
+    """Decode 16-bit patterns to float64 the way the oracle does."""
+    lib = _load()
+    t = _TYPE_CODES[type_ab]
+    b = np.asarray(bits, dtype=np.uint16)
+    out = np.fromiter((lib.oracle_decode16(int(v), t) for v in b.ravel()),
+                      dtype=np.float64, count=b.size)
+    return out.reshape(b.shape)
+
+
+def tolerance(c_ref, bnd, c_in, *, alpha, beta, out_bf16):
+    """Acceptance bound per element: 1e-5*|alpha|*Bnd + 1e-5*|beta*C_in|,
+    plus 2^-8*|C_ref| (one bf16 rounding, 8-bit significand) for bf16 output.
+    With alpha=1, beta=0 and fp32 output this is the stated 1e-5*sum|a||b|."""
+    tol = 1e-5 * abs(alpha) * bnd
+    if beta != 0.0 and c_in is not None:
+        tol = tol + 1e-5 * abs(beta) * np.abs(c_in)
+    if out_bf16:
+        tol = tol + 2.0 ** -8 * np.abs(c_ref)
+    return tol
