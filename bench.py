@@ -1,0 +1,482 @@
+"""Benchmark of the batched dense product on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+A step is one call of the product over the workload's whole batch, through
+the C ABI (bmm_run) with inputs resident in HBM.  The default workload is the
+square GEMM the headline metric is quoted on: batch 1, M = N = K = 4096,
+A row-major, B column-major (transB), bf16 normal(0,1) inputs, fp32
+accumulation, bf16 output, alpha = 1, beta = 0.  Its working set (96 MB) fits
+in the 129 MB L2, so a 512 MB buffer is written between timed steps to
+evict L2; the flush is outside the timed interval.
+
+Prints one JSON line (rank 0).  ``roofline`` compares the dominant kernel's
+algorithmic FLOP/s (2*M*N*K per launch over its CUDA-event duration) with the
+measured dense bf16 peak; ``e2e`` repeats the metric with host buffers (H2D of
+A and B from pinned memory, the call, D2H of C inside each timed step);
+``cpu_baseline`` times the fp64 oracle on the host cores on a bounded sample
+of the same workload.  ``other_workloads`` reports the remaining specified
+shapes (ragged, attention pair, skinny, small) measured the same way.
+
+With ``--impl reference`` the reference arm runs instead: the fp64 CPU
+oracle, timed on this host's cores on a bounded sample of each step.
+Multi-GPU (torchrun): every rank runs its own copy of the workload
+(independent problems, no collective on the data path); value = all ranks'
+FLOPs over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+# Denominators measured on the GB300s (copy of MEASURED_PEAKS.json,
+# 2026-12-02): read live when the file is present.
+MEASURED_FALLBACK = {"hbm_gbs": 6676.5, "bf16_tflops": 1932.9, "bf16_tflops_sustained": 1743.9,
+                     "sm_max_mhz": 2070.0}
+RECIPE_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# DRAM traffic per launch of the dominant kernel from one ncu capture, keyed by
+# a hash of the kernel sources: reported only while the sources are unchanged.
+NCU_TRAFFIC = {}
+
+FLUSH_BYTES = 512 << 20
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "dense_matmul_tensor_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh")):
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            d = json.load(open(path))
+            return {k: float(d[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained")}, \
+                "measured"
+        except Exception:
+            pass
+    return dict(MEASURED_FALLBACK), "measured (copied from this pool's MEASURED_PEAKS.json)"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="gemm_4096x4096x4096_tn_bf16")
+    ap.add_argument("--no-other", action="store_true", help="skip the other workloads")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the cpu_baseline leg")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons (every 100 ms)."""
+
+    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str):
+        self.uuid = uuid.lower()
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu=timestamp,{self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-f", self.path], stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except FileNotFoundError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def samples(self):
+        out = []
+        if not self.path or not os.path.exists(self.path):
+            return out
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 10:
+                continue
+            ts, uuid = parts[0], parts[1].lower()
+            if self.uuid and self.uuid not in uuid:
+                continue
+            try:
+                t = time.mktime(time.strptime(ts.split(".")[0], "%Y/%m/%d %H:%M:%S")) + \
+                    float("0." + ts.split(".")[1]) if "." in ts else 0.0
+            except Exception:
+                t = 0.0
+            out.append(dict(t=t, sm=float(parts[2]), sm_max=float(parts[3]),
+                            power=float(parts[4]) if parts[4].replace(".", "").isdigit() else None,
+                            hw_slowdown=parts[6], hw_thermal=parts[7], sw_thermal=parts[8],
+                            sw_power_cap=parts[9]))
+        return out
+
+    def summary(self, t0, t1):
+        s = self.samples()
+        window = [x for x in s if t0 - 0.15 <= x["t"] <= t1 + 0.15]
+        used = window or ([min(s, key=lambda x: abs(x["t"] - (t0 + t1) / 2))] if s else [])
+        if not used:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        reasons = set()
+        for x in used:
+            for k, name in (("hw_slowdown", "hw_slowdown"), ("hw_thermal", "hw_thermal_slowdown"),
+                            ("sw_thermal", "sw_thermal_slowdown"), ("sw_power_cap", "sw_power_cap")):
+                if x[k].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(x["sm"] for x in used),
+                "sm_max_mhz": max(x["sm_max"] for x in used), "reasons": sorted(reasons),
+                "samples": len(window), "nearest_only": not window}
+
+
+# ---------------------------------------------------------- our GPU arm
+
+def gpu_inputs(p, dev, seed):
+    """Seeded synthetic inputs drawn on the device (same distributions as the
+    host generator; used only where values do not enter a parity check)."""
+    import torch
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    dt = torch.bfloat16 if p.type_ab == "bf16" else torch.float16
+    na, nb, nc = p.storage_elems()
+
+    def draw(n, dist):
+        if dist == "uniform":
+            return (torch.rand(n, generator=g, device=dev, dtype=torch.float32) * 2 - 1).to(dt)
+        return torch.randn(n, generator=g, device=dev, dtype=torch.float32).to(dt)
+
+    A, B = draw(na, p.dist_ab), draw(nb, p.dist_ab)
+    if p.name.startswith("attn_pv"):
+        # P rows are softmax rows of N(0,1) scores, as in the attention pair
+        A = torch.softmax(torch.randn(p.batch * p.M, p.K, generator=g, device=dev), dim=1).to(dt)
+        A = A.reshape(-1)
+    cdt = torch.float32 if p.type_c == "f32" else torch.bfloat16
+    if p.beta != 0.0:
+        C = draw(nc, p.dist_c).to(cdt)
+    else:
+        C = torch.empty(nc, dtype=cdt, device=dev)
+    return A, B, C
+
+
+def host_inputs(p):
+    """Seeded inputs from the shared generator module, as torch CPU tensors."""
+    import torch
+    from dense_matmul_tensor_gb300 import workloads as wl
+    x = wl.make_inputs(p)
+    A = wl.as_torch16(x.A, p.type_ab)
+    B = wl.as_torch16(x.B, p.type_ab)
+    nc = p.storage_elems()[2]
+    if x.C_in is not None:
+        C = torch.from_numpy(x.C_in) if p.type_c == "f32" else wl.as_torch16(x.C_in, "bf16")
+    else:
+        C = torch.zeros(nc, dtype=torch.float32 if p.type_c == "f32" else torch.bfloat16)
+    return A, B, C
+
+
+def desc_of(p):
+    from dense_matmul_tensor_gb300 import bmm
+    s = p.strides()
+    return bmm.make_desc(batch=p.batch, M=p.M, N=p.N, K=p.K, lda=s["lda"], ldb=s["ldb"],
+                         ldc=s["ldc"], strideA=s["sA"], strideB=s["sB"], strideC=s["sC"],
+                         transA=p.transA, transB=p.transB, typeA=p.type_ab, typeC=p.type_c)
+
+
+def time_device(p, A, B, C, steps, warmup, flush, stream, barrier):
+    """Per-step CUDA-event times (ms) of bmm_run with resident inputs."""
+    import torch
+    from dense_matmul_tensor_gb300 import bmm
+    plan = bmm.Plan(desc_of(p))
+    info = plan.info()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            flush.fill_(i & 0xFF)
+            plan.run(A, B, C, p.alpha, p.beta, stream)
+    torch.cuda.synchronize()
+    st, word = plan.device_error()
+    if st != bmm.BMM_OK:
+        raise RuntimeError(f"device error {word:#x} during warm-up")
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    with torch.cuda.stream(stream):
+        for i in range(steps):
+            flush.fill_(i & 0xFF)
+            ev[i][0].record(stream)
+            plan.run(A, B, C, p.alpha, p.beta, stream)
+            ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    t1 = time.time()
+    st, word = plan.device_error()
+    plan.close()
+    if st != bmm.BMM_OK:
+        raise RuntimeError(f"device error {word:#x} in the timed region")
+    ms = [a.elapsed_time(b) for a, b in ev]
+    launches = 1 + int(info.pack_a) + int(info.pack_b)
+    return ms, info, launches, (t0, t1)
+
+
+def time_e2e(p, steps, warmup, stream, dev):
+    """Metric through the C ABI with host buffers: per step H2D of A and B
+    from pinned memory, the call, D2H of C; CUDA events around all three."""
+    import torch
+    from dense_matmul_tensor_gb300 import bmm
+    hA, hB, hC = host_inputs(p)
+    hA, hB, hC = hA.pin_memory(), hB.pin_memory(), hC.pin_memory()
+    dA = torch.empty_like(hA, device=dev)
+    dB = torch.empty_like(hB, device=dev)
+    dC = torch.empty_like(hC, device=dev)
+    out = torch.empty_like(hC).pin_memory()
+    plan = bmm.Plan(desc_of(p))
+
+    def step():
+        dA.copy_(hA, non_blocking=True)
+        dB.copy_(hB, non_blocking=True)
+        if p.beta != 0.0:
+            dC.copy_(hC, non_blocking=True)
+        plan.run(dA, dB, dC, p.alpha, p.beta, stream)
+        out.copy_(dC, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            step()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    plan.close()
+    ms = e0.elapsed_time(e1) / steps
+    h2d = hA.numel() * hA.element_size() + hB.numel() * hB.element_size() + \
+        (hC.numel() * hC.element_size() if p.beta != 0.0 else 0)
+    d2h = hC.numel() * hC.element_size()
+    return ms, h2d, d2h
+
+
+def metric_value(p, ms):
+    return p.flops() / (ms * 1e-3) / 1e12  # TFLOP/s
+
+
+# ------------------------------------------------------------ CPU oracle
+
+class OracleSample:
+    """The fp64 oracle on the first ``rows`` rows of C (batch item 0, full N
+    and K).  ``calibrate`` picks ``rows`` from a short probe so that one run
+    takes about ``target_s`` seconds."""
+
+    def __init__(self, p, threads=None):
+        import oracle
+        from dense_matmul_tensor_gb300 import workloads as wl
+        self.oracle = oracle
+        self.p = p
+        self.x = wl.make_inputs(wl.Problem(**{**p.__dict__, "batch": 1}))
+        self.cores = threads or oracle.host_threads()
+        self.kw = dict(p.oracle_kwargs(), batch=1)
+        self.rows = max(1, min(p.M, 32))
+
+    def run(self, rows=None):
+        rows = rows or self.rows
+        k = dict(self.kw, M=rows)
+        A = self.x.A if self.p.transA else self.x.A[: rows * self.kw["lda"]]
+        t = time.perf_counter()
+        self.oracle.bmm(A, self.x.B, self.x.C_in, threads=self.cores, **k)
+        dt = time.perf_counter() - t
+        return 2.0 * rows * self.p.N * self.p.K / dt / 1e12, dt
+
+    def calibrate(self, target_s):
+        probe = max(1, min(self.p.M, 32))
+        _, dt = self.run(probe)
+        self.rows = int(max(1, min(self.p.M, round(probe / max(dt, 1e-6) * target_s))))
+        return self.rows
+
+
+# ------------------------------------------------------------------ main
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_env()
+    from dense_matmul_tensor_gb300 import workloads as wl
+    p = wl.WORKLOADS[args.workload]
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        total = args.steps + args.warmup
+        sampler = OracleSample(p)
+        rows = sampler.calibrate(max(0.02, min(10.0, 120.0 / max(total, 1))))
+        cores = sampler.cores
+        vals = []
+        for i in range(total):
+            v, dt = sampler.run()
+            if i >= args.warmup:
+                vals.append((v, dt))
+        value = statistics.median(v for v, _ in vals)
+        ms = statistics.median(dt for _, dt in vals) * 1e3
+        line = {"impl": "reference", "metric": "BMM TFLOP/s (bf16 in, fp32 accumulate)",
+                "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": {"workload": p.name, "batch": p.batch, "M": p.M, "N": p.N, "K": p.K,
+                           "transA": p.transA, "transB": p.transB, "inputs": p.type_ab,
+                           "output": p.type_c},
+                "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                                 "sample": f"first {rows} of {p.M} rows of C per step (fp64 oracle, "
+                                           f"{cores} threads)"},
+                "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+
+    import torch
+    import torch.distributed as dist
+    from dense_matmul_tensor_gb300 import bmm
+
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    bmm.load_library()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    def max_over_ranks(x):
+        if world == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    peaks, peak_src = load_peaks()
+    stream = torch.cuda.Stream(device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    A, B, C = (t.to(dev) for t in host_inputs(p))
+
+    props = torch.cuda.get_device_properties(dev)
+    clocks = ClockSampler(str(getattr(props, "uuid", "")))
+    clocks.start()
+    ms_list, info, launches, (t0, t1) = time_device(p, A, B, C, args.steps, max(args.warmup, 3),
+                                                     flush, stream, barrier)
+    clocks.stop()
+    ms_mean = statistics.fmean(ms_list)
+    ms_step = max_over_ranks(ms_mean)
+    value = world * p.flops() / (ms_step * 1e-3) / 1e12
+
+    achieved = p.flops() / (ms_mean * 1e-3) / 1e12
+    roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+            "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+            "traffic": NCU_TRAFFIC.get(kernel_source_hash()),
+            "kernel": f"bmm_tc_kernel<{info.tile_n}>", "peak_source": f"{peak_src} bf16 burst",
+            "algorithmic_flops_per_launch": p.flops(),
+            "ms_per_launch_median": statistics.median(ms_list),
+            "achieved_median": p.flops() / (statistics.median(ms_list) * 1e-3) / 1e12}
+
+    line = {"metric": "BMM TFLOP/s & % of GB300 bf16 tensor peak; GB/s & % HBM for skinny shapes",
+            "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": max(args.warmup, 3), "ms_per_step": ms_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": p.name, "batch": p.batch, "M": p.M, "N": p.N, "K": p.K,
+                       "transA": p.transA, "transB": p.transB, "inputs": f"{p.type_ab} {p.dist_ab}",
+                       "output": p.type_c, "alpha": p.alpha, "beta": p.beta,
+                       "l2": f"flushed: {FLUSH_BYTES >> 20} MB write between timed steps",
+                       "tile": [info.tile_m, info.tile_n, info.tile_k], "stages": info.stages,
+                       "parallelism": f"{world} independent replicas" if world > 1 else "1 GPU"},
+            "roofline": roof,
+            "gpu_launches": launches * args.steps,
+            "clocks": clocks.summary(t0, t1)}
+
+    if not args.no_e2e:
+        e2e_steps = max(5, min(args.steps, 50))
+        ms_e, h2d, d2h = time_e2e(p, e2e_steps, 3, stream, dev)
+        ms_e = max_over_ranks(ms_e)
+        line["e2e"] = {"value": world * p.flops() / (ms_e * 1e-3) / 1e12, "unit": "TFLOP/s",
+                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                       "ms_per_step": ms_e}
+
+    if not args.no_other:
+        other = []
+        for name, q in wl.WORKLOADS.items():
+            if name == p.name:
+                continue
+            qa, qb, qc = gpu_inputs(q, dev, 1000 * q.seed)
+            torch.cuda.synchronize()
+            qs = min(args.steps, 20)
+            mq, qinfo, _, _ = time_device(q, qa, qb, qc, qs, 3, flush, stream, lambda: None)
+            mqm = statistics.fmean(mq)
+            gbs = q.algorithmic_bytes() / (mqm * 1e-3) / 1e9
+            tf = q.flops() / (mqm * 1e-3) / 1e12
+            other.append({"workload": name, "ms": mqm, "TFLOP/s": tf,
+                          "frac_bf16_peak": tf / peaks["bf16_tflops"], "GB/s": gbs,
+                          "frac_hbm": gbs / peaks["hbm_gbs"],
+                          "intensity_flop_per_byte": q.flops() / q.algorithmic_bytes(),
+                          "tile_n": qinfo.tile_n, "swap_ab": qinfo.swap_ab,
+                          "pack": [qinfo.pack_a, qinfo.pack_b]})
+            del qa, qb, qc
+            torch.cuda.empty_cache()
+        line["other_workloads"] = other
+
+    if rank == 0 and not args.no_cpu:
+        sampler = OracleSample(p)
+        rows = sampler.calibrate(15.0)
+        v, dt = sampler.run()
+        cores = sampler.cores
+        line["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                                "sample": f"first {rows} of {p.M} rows of C, full N and K "
+                                          f"({2 * rows * p.N * p.K / 1e9:.1f} GFLOP in {dt:.1f} s)"}
+    if world > 1:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

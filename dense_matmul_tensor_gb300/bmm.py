@@ -1,0 +1,199 @@
+"""Thin ctypes binding of the C ABI in ``include/bmm.h`` (same names).
+
+Argument marshalling only: every step of the product runs in the CUDA
+kernels of ``libdmt_bmm.so``.  Device pointers may be passed as integers or
+as any object with ``data_ptr()`` (a torch tensor); streams as an integer
+handle, an object with ``cuda_stream`` (a torch stream), or None.  There is
+no fallback: if the library is not built, the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import build as _build
+
+BMM_BF16, BMM_F16, BMM_F32 = 0, 1, 2
+DTYPES = {"bf16": BMM_BF16, "f16": BMM_F16, "f32": BMM_F32}
+
+BMM_OK = 0
+BMM_ERR_INVALID_ARG = 1
+BMM_ERR_UNSUPPORTED = 2
+BMM_ERR_MISALIGNED = 3
+BMM_ERR_CUDA = 4
+BMM_ERR_DEVICE_TIMEOUT = 5
+BMM_ERR_NO_DEVICE = 6
+
+EXPORTED = ("bmm_create", "bmm_plan_query", "bmm_get_plan_info", "bmm_run",
+            "bmm_get_device_error", "bmm_destroy", "bmm_status_string", "bmm_version")
+
+
+class bmm_desc_t(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int64) for n in
+                ("batch", "M", "N", "K", "lda", "ldb", "ldc", "strideA", "strideB", "strideC")] + \
+               [(n, ctypes.c_int32) for n in ("transA", "transB", "typeA", "typeB", "typeC")]
+
+
+class bmm_plan_info_t(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in
+                ("tile_m", "tile_n", "tile_k", "stages", "swap_ab", "pack_a", "pack_b", "even_k",
+                 "tmem_cols")] + \
+               [(n, ctypes.c_int64) for n in
+                ("tiles", "smem_bytes", "stage_bytes", "workspace_bytes")]
+
+    def as_dict(self):
+        return {n: getattr(self, n) for n, _ in self._fields_}
+
+
+class BmmError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {bmm_status_string(status)} ({status})")
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load_library() -> ctypes.CDLL:
+    """Load ``libdmt_bmm.so``; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"GPU library not built: {path} is missing "
+                           "(run dense_matmul_tensor_gb300.build.build())")
+    lib = ctypes.CDLL(path)
+    P = ctypes.POINTER
+    vp = ctypes.c_void_p
+    lib.bmm_create.argtypes = [P(bmm_desc_t), P(vp)]
+    lib.bmm_create.restype = ctypes.c_int
+    lib.bmm_plan_query.argtypes = [P(bmm_desc_t), P(bmm_plan_info_t)]
+    lib.bmm_plan_query.restype = ctypes.c_int
+    lib.bmm_get_plan_info.argtypes = [vp, P(bmm_plan_info_t)]
+    lib.bmm_get_plan_info.restype = ctypes.c_int
+    lib.bmm_run.argtypes = [vp, vp, vp, vp, ctypes.c_float, ctypes.c_float, vp]
+    lib.bmm_run.restype = ctypes.c_int
+    lib.bmm_get_device_error.argtypes = [vp, P(ctypes.c_uint32)]
+    lib.bmm_get_device_error.restype = ctypes.c_int
+    lib.bmm_destroy.argtypes = [vp]
+    lib.bmm_destroy.restype = ctypes.c_int
+    lib.bmm_status_string.argtypes = [ctypes.c_int]
+    lib.bmm_status_string.restype = ctypes.c_char_p
+    lib.bmm_version.argtypes = []
+    lib.bmm_version.restype = ctypes.c_int32
+    _lib = lib
+    return lib
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if hasattr(x, "data_ptr"):
+        return ctypes.c_void_p(x.data_ptr())
+    return ctypes.c_void_p(int(x))
+
+
+def _stream(s):
+    if s is None:
+        return None
+    if hasattr(s, "cuda_stream"):
+        return ctypes.c_void_p(s.cuda_stream)
+    return ctypes.c_void_p(int(s))
+
+
+def make_desc(*, batch, M, N, K, lda, ldb, ldc, strideA, strideB, strideC, transA=0, transB=0,
+              typeA="bf16", typeB=None, typeC="f32") -> bmm_desc_t:
+    t = lambda v: DTYPES[v] if isinstance(v, str) else int(v)  # noqa: E731
+    return bmm_desc_t(batch, M, N, K, lda, ldb, ldc, strideA, strideB, strideC, int(transA),
+                      int(transB), t(typeA), t(typeB if typeB is not None else typeA), t(typeC))
+
+
+def bmm_status_string(status: int) -> str:
+    return load_library().bmm_status_string(int(status)).decode()
+
+
+def bmm_version() -> int:
+    return load_library().bmm_version()
+
+
+def bmm_plan_query(desc: bmm_desc_t) -> bmm_plan_info_t:
+    info = bmm_plan_info_t()
+    st = load_library().bmm_plan_query(ctypes.byref(desc), ctypes.byref(info))
+    if st != BMM_OK:
+        raise BmmError(st, "bmm_plan_query")
+    return info
+
+
+def bmm_create(desc: bmm_desc_t) -> ctypes.c_void_p:
+    plan = ctypes.c_void_p()
+    st = load_library().bmm_create(ctypes.byref(desc), ctypes.byref(plan))
+    if st != BMM_OK:
+        raise BmmError(st, "bmm_create")
+    return plan
+
+
+def bmm_get_plan_info(plan) -> bmm_plan_info_t:
+    info = bmm_plan_info_t()
+    st = load_library().bmm_get_plan_info(plan, ctypes.byref(info))
+    if st != BMM_OK:
+        raise BmmError(st, "bmm_get_plan_info")
+    return info
+
+
+def bmm_run(plan, A, B, C, alpha=1.0, beta=0.0, stream=None) -> None:
+    st = load_library().bmm_run(plan, _ptr(A), _ptr(B), _ptr(C), float(alpha), float(beta),
+                                _stream(stream))
+    if st != BMM_OK:
+        raise BmmError(st, "bmm_run")
+
+
+def bmm_get_device_error(plan):
+    """Returns (status, raw_word); call after the stream has been synchronised."""
+    w = ctypes.c_uint32(0)
+    st = load_library().bmm_get_device_error(plan, ctypes.byref(w))
+    return st, w.value
+
+
+def bmm_destroy(plan) -> None:
+    st = load_library().bmm_destroy(plan)
+    if st != BMM_OK:
+        raise BmmError(st, "bmm_destroy")
+
+
+class Plan:
+    """Owns one plan: ``with Plan(desc) as p: p.run(A, B, C, alpha, beta, stream)``."""
+
+    def __init__(self, desc: bmm_desc_t):
+        self.desc = desc
+        self.handle = bmm_create(desc)
+
+    def run(self, A, B, C, alpha=1.0, beta=0.0, stream=None):
+        bmm_run(self.handle, A, B, C, alpha, beta, stream)
+
+    def info(self) -> bmm_plan_info_t:
+        return bmm_get_plan_info(self.handle)
+
+    def device_error(self):
+        return bmm_get_device_error(self.handle)
+
+    def close(self):
+        if self.handle:
+            bmm_destroy(self.handle)
+            self.handle = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

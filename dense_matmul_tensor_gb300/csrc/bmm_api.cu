@@ -1,0 +1,442 @@
+// C ABI of the batched product (declared in include/bmm.h): validation,
+// planning, tensor-map encoding and kernel launches.  All compute runs in the
+// kernels of bmm_kernel.cuh; this file only decides and enqueues.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include "../../include/bmm.h"
+#include "bmm_kernel.cuh"
+
+namespace {
+
+using dmt::KParams;
+
+constexpr int32_t kVersion = (0 << 16) | 1;
+constexpr int kGb300Sms = 152;
+constexpr int64_t kMaxDim = 0x7fffffffLL;
+
+// One MMA operand (A = rows of D, B = columns of D) as it sits in memory.
+struct Operand {
+  int user;          // 0: the caller's A, 1: the caller's B
+  int mn_major;      // 1: the MMA's M (or N) index is the contiguous one
+  int64_t rows, cols;// stored matrix per batch item (row-major, `ld`)
+  int64_t ld, stride;
+  int bcast;         // one batch item shared by all
+  int pack;          // staged into the workspace first
+  int64_t pld, pstride, ws_off;
+  int box_rows;      // TMA box rows for a K-major operand (128 or BN)
+};
+
+struct Planned {
+  int swap;
+  int64_t batch, Mv, Nv, K;
+  Operand a, b;
+  int bn, stages;
+  uint32_t stage_bytes, a_bytes, tx_bytes, idesc, tmem_cols;
+  int64_t tiles, smem_bytes, workspace_bytes;
+  int32_t num_m, num_n, k_blocks, tail_steps;
+};
+
+int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+
+bool is16(int32_t t) { return t == BMM_BF16 || t == BMM_F16; }
+
+bmm_status_t validate(const bmm_desc_t* d) {
+  if (!d) return BMM_ERR_INVALID_ARG;
+  if (d->batch < 0 || d->M < 0 || d->N < 0 || d->K < 0) return BMM_ERR_INVALID_ARG;
+  if (d->transA != 0 && d->transA != 1) return BMM_ERR_INVALID_ARG;
+  if (d->transB != 0 && d->transB != 1) return BMM_ERR_INVALID_ARG;
+  if (!is16(d->typeA) || d->typeB != d->typeA) return BMM_ERR_INVALID_ARG;
+  if (d->typeC != BMM_F32 && d->typeC != BMM_BF16) return BMM_ERR_INVALID_ARG;
+  if (d->strideA < 0 || d->strideB < 0 || d->strideC < 0) return BMM_ERR_INVALID_ARG;
+  const int64_t a_cols = d->transA ? d->M : d->K;
+  const int64_t b_cols = d->transB ? d->K : d->N;
+  if (d->lda < (a_cols > 1 ? a_cols : 1)) return BMM_ERR_INVALID_ARG;
+  if (d->ldb < (b_cols > 1 ? b_cols : 1)) return BMM_ERR_INVALID_ARG;
+  if (d->ldc < (d->N > 1 ? d->N : 1)) return BMM_ERR_INVALID_ARG;
+  if (d->batch > 1 && d->M > 0 && d->N > 0 && d->strideC < (d->M - 1) * d->ldc + d->N)
+    return BMM_ERR_INVALID_ARG;  // batch items of C would overlap
+  if (d->batch > kMaxDim || d->M > kMaxDim || d->N > kMaxDim || d->K > kMaxDim)
+    return BMM_ERR_UNSUPPORTED;
+  return BMM_OK;
+}
+
+// Shape classes and resources.  Pure host arithmetic (no CUDA calls).
+void plan(const bmm_desc_t* d, Planned* P) {
+  std::memset(P, 0, sizeof(*P));
+  // Skinny M: compute C^T = op(B)^T op(A)^T so that N fills the 128-row MMA.
+  P->swap = (d->M <= 64 && d->N > d->M) ? 1 : 0;
+  P->batch = d->batch;
+  P->K = d->K;
+  Operand ua{}, ub{};
+  ua.user = 0;
+  ua.rows = d->transA ? d->K : d->M;
+  ua.cols = d->transA ? d->M : d->K;
+  ua.ld = d->lda;
+  ua.stride = d->strideA;
+  ub.user = 1;
+  ub.rows = d->transB ? d->N : d->K;
+  ub.cols = d->transB ? d->K : d->N;
+  ub.ld = d->ldb;
+  ub.stride = d->strideB;
+  if (!P->swap) {
+    P->Mv = d->M;
+    P->Nv = d->N;
+    P->a = ua;
+    P->b = ub;
+    P->a.mn_major = d->transA ? 1 : 0;  // A stored K x M: M contiguous
+    P->b.mn_major = d->transB ? 0 : 1;  // B stored K x N: N contiguous
+  } else {
+    P->Mv = d->N;
+    P->Nv = d->M;
+    P->a = ub;
+    P->b = ua;
+    P->a.mn_major = d->transB ? 0 : 1;
+    P->b.mn_major = d->transA ? 1 : 0;
+  }
+  // Tile N: the smallest of 16..256 that covers Nv.  An MN-major B tile is
+  // loaded in 64-wide boxes (one 128-byte swizzle row), so it needs BN >= 64.
+  int bn = 256;
+  if (P->Nv <= 16 && !P->b.mn_major) bn = 16;
+  else if (P->Nv <= 32 && !P->b.mn_major) bn = 32;
+  else if (P->Nv <= 64) bn = 64;
+  else if (P->Nv <= 128) bn = 128;
+  P->bn = bn;
+  P->a.box_rows = dmt::kTileM;
+  P->b.box_rows = bn;
+
+  // TMA needs 16-byte row and batch strides; otherwise stage a copy with
+  // ld rounded up to 8 elements.
+  int64_t ws = 0;
+  for (Operand* o : {&P->a, &P->b}) {
+    o->bcast = (o->stride == 0 || d->batch <= 1) ? 1 : 0;
+    const bool ld_ok = (o->ld * 2) % 16 == 0;
+    const bool st_ok = o->bcast || (o->stride * 2) % 16 == 0;
+    o->pack = (ld_ok && st_ok) ? 0 : 1;
+    if (o->pack) {
+      o->pld = round_up(o->cols, 8);
+      o->pstride = o->rows * o->pld;
+      o->ws_off = ws;
+      const int64_t nb = o->bcast ? 1 : d->batch;
+      ws = round_up(ws + nb * o->pstride * 2, 256);
+    }
+  }
+  P->workspace_bytes = ws;
+
+  P->a_bytes = static_cast<uint32_t>(dmt::kTileM * dmt::kTileK * 2);
+  const uint32_t b_bytes = static_cast<uint32_t>(bn * dmt::kTileK * 2);
+  P->stage_bytes = static_cast<uint32_t>(round_up(P->a_bytes + b_bytes, 1024));
+  P->tx_bytes = P->a_bytes + b_bytes;
+  const int64_t fixed = 1024 + dmt::kEpiBytes + dmt::kBarBytes;
+  int stages = static_cast<int>((dmt::kSmemLimit - fixed) / P->stage_bytes);
+  if (stages > 16) stages = 16;
+  P->stages = stages;
+  P->smem_bytes = fixed + static_cast<int64_t>(stages) * P->stage_bytes;
+
+  uint32_t cols = 32;
+  while (cols < static_cast<uint32_t>(2 * bn)) cols <<= 1;
+  P->tmem_cols = cols;
+
+  const uint32_t fmt = (d->typeA == BMM_BF16) ? 1u : 0u;  // 0 = fp16, 1 = bf16
+  P->idesc = (1u << 4)                                   // D format: fp32
+             | (fmt << 7) | (fmt << 10)                  // A and B formats
+             | (static_cast<uint32_t>(P->a.mn_major) << 15) |
+             (static_cast<uint32_t>(P->b.mn_major) << 16) |
+             (static_cast<uint32_t>(bn >> 3) << 17)      // N / 8
+             | (static_cast<uint32_t>(dmt::kTileM >> 4) << 24);  // M / 16
+
+  P->num_m = static_cast<int32_t>((P->Mv + dmt::kTileM - 1) / dmt::kTileM);
+  P->num_n = static_cast<int32_t>((P->Nv + bn - 1) / bn);
+  P->tiles = P->batch * P->num_m * P->num_n;
+  P->k_blocks = static_cast<int32_t>((P->K + dmt::kTileK - 1) / dmt::kTileK);
+  const int64_t rem = P->K % dmt::kTileK;
+  P->tail_steps = rem == 0 ? dmt::kTileK / dmt::kUmmaK
+                           : static_cast<int32_t>((rem + dmt::kUmmaK - 1) / dmt::kUmmaK);
+}
+
+void fill_info(const Planned& P, const bmm_desc_t* d, bmm_plan_info_t* info) {
+  std::memset(info, 0, sizeof(*info));
+  info->tile_m = dmt::kTileM;
+  info->tile_n = P.bn;
+  info->tile_k = dmt::kTileK;
+  info->stages = P.stages;
+  info->swap_ab = P.swap;
+  info->pack_a = P.swap ? P.b.pack : P.a.pack;
+  info->pack_b = P.swap ? P.a.pack : P.b.pack;
+  info->even_k = (d->K % dmt::kTileK) == 0 ? 1 : 0;
+  info->tmem_cols = static_cast<int32_t>(P.tmem_cols);
+  info->tiles = P.tiles;
+  info->smem_bytes = P.smem_bytes;
+  info->stage_bytes = P.stage_bytes;
+  info->workspace_bytes = P.workspace_bytes;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool get_encoder() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode != nullptr;
+}
+
+template <int BN>
+bool prepare_kernel(int64_t smem) {
+  static std::once_flag once;
+  static bool ok = false;
+  std::call_once(once, [] {
+    ok = cudaFuncSetAttribute(dmt::bmm_tc_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(dmt::kSmemLimit)) == cudaSuccess;
+  });
+  (void)smem;
+  return ok;
+}
+
+uint64_t wait_timeout_ns() {
+  const char* e = std::getenv("DMT_BMM_WAIT_TIMEOUT_MS");
+  if (e && *e) {
+    const long long ms = std::atoll(e);
+    if (ms > 0) return static_cast<uint64_t>(ms) * 1000000ull;
+  }
+  return 2000000000ull;  // 2 s
+}
+
+}  // namespace
+
+struct bmm_plan_s {
+  bmm_desc_t d;
+  Planned P;
+  int device;
+  int sms;
+  void* ws;
+  uint32_t* err;
+  uint64_t timeout_ns;
+  const void* map_ptr[2];
+  CUtensorMap map[2];
+};
+
+namespace {
+
+bool encode_map(const bmm_plan_s* pl, const Operand& o, const void* base, CUtensorMap* out) {
+  const int64_t ld = o.pack ? o.pld : o.ld;
+  const int64_t stride = o.pack ? o.pstride : o.stride;
+  const int64_t nb = o.bcast ? 1 : pl->P.batch;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(o.cols), static_cast<cuuint64_t>(o.rows),
+                        static_cast<cuuint64_t>(nb)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld * 2),
+                           static_cast<cuuint64_t>(nb > 1 ? stride * 2 : round_up(o.rows * ld * 2, 16))};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(dmt::kTileK),
+                       static_cast<cuuint32_t>(o.mn_major ? 64 : o.box_rows), 1u};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  const CUtensorMapDataType dt = pl->d.typeA == BMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                          : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const CUresult r = g_encode(out, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int BN>
+cudaError_t launch_gemm(const bmm_plan_s* pl, const KParams& kp, cudaStream_t stream) {
+  if (!prepare_kernel<BN>(pl->P.smem_bytes)) return cudaErrorInvalidValue;
+  int64_t grid = pl->P.tiles < pl->sms ? pl->P.tiles : pl->sms;
+  dmt::bmm_tc_kernel<BN><<<static_cast<unsigned>(grid), dmt::kThreads,
+                           static_cast<size_t>(pl->P.smem_bytes), stream>>>(kp, pl->map[0],
+                                                                           pl->map[1]);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t bmm_version(void) { return kVersion; }
+
+const char* bmm_status_string(bmm_status_t s) {
+  switch (s) {
+    case BMM_OK: return "BMM_OK";
+    case BMM_ERR_INVALID_ARG: return "BMM_ERR_INVALID_ARG";
+    case BMM_ERR_UNSUPPORTED: return "BMM_ERR_UNSUPPORTED";
+    case BMM_ERR_MISALIGNED: return "BMM_ERR_MISALIGNED";
+    case BMM_ERR_CUDA: return "BMM_ERR_CUDA";
+    case BMM_ERR_DEVICE_TIMEOUT: return "BMM_ERR_DEVICE_TIMEOUT";
+    case BMM_ERR_NO_DEVICE: return "BMM_ERR_NO_DEVICE";
+  }
+  return "BMM_ERR_UNKNOWN";
+}
+
+bmm_status_t bmm_plan_query(const bmm_desc_t* desc, bmm_plan_info_t* info) {
+  if (!info) return BMM_ERR_INVALID_ARG;
+  const bmm_status_t st = validate(desc);
+  if (st != BMM_OK) return st;
+  Planned P;
+  plan(desc, &P);
+  fill_info(P, desc, info);
+  (void)kGb300Sms;
+  return BMM_OK;
+}
+
+bmm_status_t bmm_create(const bmm_desc_t* desc, bmm_plan_t* out) {
+  if (!out) return BMM_ERR_INVALID_ARG;
+  *out = nullptr;
+  const bmm_status_t st = validate(desc);
+  if (st != BMM_OK) return st;
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return BMM_ERR_NO_DEVICE;
+  int major = 0, minor = 0, sms = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return BMM_ERR_NO_DEVICE;
+  if (major != 10 || minor != 3) return BMM_ERR_NO_DEVICE;  // built for sm_103a only
+  if (!get_encoder()) return BMM_ERR_CUDA;
+
+  bmm_plan_s* pl = new (std::nothrow) bmm_plan_s();
+  if (!pl) return BMM_ERR_CUDA;
+  pl->d = *desc;
+  plan(desc, &pl->P);
+  pl->device = dev;
+  pl->sms = sms;
+  pl->timeout_ns = wait_timeout_ns();
+  if (cudaMalloc(reinterpret_cast<void**>(&pl->err), 256) != cudaSuccess ||
+      cudaMemset(pl->err, 0, 256) != cudaSuccess) {
+    cudaFree(pl->err);
+    delete pl;
+    return BMM_ERR_CUDA;
+  }
+  if (pl->P.workspace_bytes > 0 &&
+      cudaMalloc(&pl->ws, static_cast<size_t>(pl->P.workspace_bytes)) != cudaSuccess) {
+    cudaFree(pl->err);
+    delete pl;
+    return BMM_ERR_CUDA;
+  }
+  *out = pl;
+  return BMM_OK;
+}
+
+bmm_status_t bmm_get_plan_info(bmm_plan_t pl, bmm_plan_info_t* info) {
+  if (!pl || !info) return BMM_ERR_INVALID_ARG;
+  fill_info(pl->P, &pl->d, info);
+  return BMM_OK;
+}
+
+bmm_status_t bmm_run(bmm_plan_t pl, const void* A, const void* B, void* C, float alpha,
+                     float beta, void* stream_v) {
+  if (!pl) return BMM_ERR_INVALID_ARG;
+  const bmm_desc_t& d = pl->d;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+  if (d.batch == 0 || d.M == 0 || d.N == 0) return BMM_OK;
+  if (!C) return BMM_ERR_INVALID_ARG;
+
+  if (alpha == 0.0f || d.K == 0) {
+    // A and B are not read: C = beta * C.
+    const int64_t rows = d.batch * d.M;
+    dim3 grid(static_cast<unsigned>((d.N + 255) / 256 < 64 ? (d.N + 255) / 256 : 64),
+              static_cast<unsigned>(rows < 65535 ? rows : 65535));
+    dmt::scale_c_kernel<<<grid, 256, 0, stream>>>(C, d.typeC == BMM_BF16, d.batch, d.M, d.N, d.ldc,
+                                                  d.strideC, beta);
+    return cudaGetLastError() == cudaSuccess ? BMM_OK : BMM_ERR_CUDA;
+  }
+  if (!A || !B) return BMM_ERR_INVALID_ARG;
+
+  const Planned& P = pl->P;
+  const void* base[2];
+  const Operand* ops[2] = {&P.a, &P.b};
+  for (int i = 0; i < 2; ++i) {
+    const Operand& o = *ops[i];
+    const void* src = o.user == 0 ? A : B;
+    if (o.pack) {
+      uint16_t* dst = reinterpret_cast<uint16_t*>(static_cast<char*>(pl->ws) + o.ws_off);
+      const int64_t nb = o.bcast ? 1 : d.batch;
+      const int64_t rows = nb * o.rows;
+      dim3 grid(static_cast<unsigned>((o.cols + 255) / 256 < 64 ? (o.cols + 255) / 256 : 64),
+                static_cast<unsigned>(rows < 65535 ? rows : 65535));
+      dmt::pack16_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(src), dst, nb,
+                                                   o.rows, o.cols, o.ld, o.bcast ? 0 : o.stride,
+                                                   o.pld, o.pstride);
+      if (cudaGetLastError() != cudaSuccess) return BMM_ERR_CUDA;
+      base[i] = dst;
+    } else {
+      if ((reinterpret_cast<uintptr_t>(src) & 15u) != 0) return BMM_ERR_MISALIGNED;
+      base[i] = src;
+    }
+    if (pl->map_ptr[i] != base[i]) {
+      if (!encode_map(pl, o, base[i], &pl->map[i])) return BMM_ERR_CUDA;
+      pl->map_ptr[i] = base[i];
+    }
+  }
+
+  KParams kp;
+  std::memset(&kp, 0, sizeof(kp));
+  kp.Mv = static_cast<int32_t>(P.Mv);
+  kp.Nv = static_cast<int32_t>(P.Nv);
+  kp.K = static_cast<int32_t>(P.K);
+  kp.num_m = P.num_m;
+  kp.num_n = P.num_n;
+  kp.tiles = P.tiles;
+  kp.k_blocks = P.k_blocks;
+  kp.tail_steps = P.tail_steps;
+  kp.a_mn = P.a.mn_major;
+  kp.b_mn = P.b.mn_major;
+  kp.a_bcast = P.a.bcast;
+  kp.b_bcast = P.b.bcast;
+  kp.stages = P.stages;
+  kp.stage_bytes = P.stage_bytes;
+  kp.a_bytes = P.a_bytes;
+  kp.tx_bytes = P.tx_bytes;
+  kp.idesc = P.idesc;
+  kp.tmem_cols = P.tmem_cols;
+  kp.C = C;
+  kp.ldc = d.ldc;
+  kp.sC = d.strideC;
+  kp.c_bf16 = d.typeC == BMM_BF16 ? 1 : 0;
+  kp.c_trans = P.swap;
+  kp.alpha = alpha;
+  kp.beta = beta;
+  kp.err = pl->err;
+  kp.timeout_ns = pl->timeout_ns;
+
+  cudaError_t e;
+  switch (P.bn) {
+    case 16: e = launch_gemm<16>(pl, kp, stream); break;
+    case 32: e = launch_gemm<32>(pl, kp, stream); break;
+    case 64: e = launch_gemm<64>(pl, kp, stream); break;
+    case 128: e = launch_gemm<128>(pl, kp, stream); break;
+    default: e = launch_gemm<256>(pl, kp, stream); break;
+  }
+  return e == cudaSuccess ? BMM_OK : BMM_ERR_CUDA;
+}
+
+bmm_status_t bmm_get_device_error(bmm_plan_t pl, uint32_t* detail) {
+  if (!pl) return BMM_ERR_INVALID_ARG;
+  uint32_t w = 0;
+  if (cudaMemcpy(&w, pl->err, sizeof(w), cudaMemcpyDeviceToHost) != cudaSuccess) return BMM_ERR_CUDA;
+  if (w != 0 && cudaMemset(pl->err, 0, sizeof(w)) != cudaSuccess) return BMM_ERR_CUDA;
+  if (detail) *detail = w;
+  return w == 0 ? BMM_OK : BMM_ERR_DEVICE_TIMEOUT;
+}
+
+bmm_status_t bmm_destroy(bmm_plan_t pl) {
+  if (!pl) return BMM_OK;
+  bmm_status_t st = BMM_OK;
+  if (pl->ws && cudaFree(pl->ws) != cudaSuccess) st = BMM_ERR_CUDA;
+  if (pl->err && cudaFree(pl->err) != cudaSuccess) st = BMM_ERR_CUDA;
+  delete pl;
+  return st;
+}
+
+}  // extern "C"

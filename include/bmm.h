@@ -1,0 +1,176 @@
+/*
+ * bmm.h — C ABI of the GB300 (sm_103a) batched dense matrix product
+ *
+ *     C[b] = alpha * op(A[b]) * op(B[b]) + beta * C[b],   b = 0 .. batch-1
+ *
+ * op() is the identity or the transpose; A and B hold bf16 or fp16 values
+ * (both the same type); products accumulate in fp32 on the tensor cores
+ * (tcgen05, accumulator in Tensor Memory); alpha and beta scale in fp32; C
+ * is stored as fp32 or bf16 (round to nearest even).
+ *
+ * Where the operation is defined:
+ *  - "Triton Optimization Reference (cuTile -> Triton)", section 1 (EVEN_K
+ *    fast path): the K loop adds tl.dot of A and B tiles into an fp32
+ *    accumulator; when K is not a multiple of the tile, the last tile's
+ *    out-of-range elements are loaded as zero.
+ *  - same page, section 2: a transposed A or B is expressed by the strides
+ *    used to address the loaded tile, never by a transpose inside the loop.
+ *  - same page, section 3: batch items are independent problems laid out
+ *    with a stride between them (batch on its own grid axis).
+ *  - "Optimize Triton Block Parameters", Correctness requirements: any tile
+ *    configuration must give the same result for M, N, K that are not
+ *    multiples of the tile (for example K = 48 with a 64-wide K tile).
+ *
+ * Storage convention (row-major, strides in ELEMENTS):
+ *   transA = 0: A[b] is M x K;  element (i,k) at A + b*strideA + i*lda + k
+ *   transA = 1: A[b] is K x M;  element (i,k) at A + b*strideA + k*lda + i
+ *   transB = 0: B[b] is K x N;  element (k,j) at B + b*strideB + k*ldb + j
+ *   transB = 1: B[b] is N x K;  element (k,j) at B + b*strideB + j*ldb + k
+ *   C[b] is M x N;              element (i,j) at C + b*strideC + i*ldc + j
+ * A batch stride of 0 broadcasts A (or B) over the batch.  C's batch stride
+ * must keep distinct batch items apart (strideC >= (M-1)*ldc + N when M > 0).
+ *
+ * Semantics:
+ *   beta == 0  -> C is not read (NaN or garbage in C does not propagate).
+ *   alpha == 0 or K == 0 -> A and B are not read; C = beta * C.
+ *   batch, M or N == 0 -> nothing is launched; BMM_OK.
+ *   C must not overlap A or B.
+ *
+ * Threading and streams: every call is host-side thread-safe for distinct
+ * plans.  One plan may have one bmm_run in flight at a time on the GPU (its
+ * operand-staging workspace and device error word are per plan).  bmm_run
+ * is asynchronous with respect to the host: it enqueues work on `stream`
+ * and returns.
+ *
+ * Errors: return codes only; nothing crosses the ABI as an exception.
+ * A device-side wait that runs past its time limit does not trap: the
+ * kernel records BMM_ERR_DEVICE_TIMEOUT in the plan's device error word,
+ * releases its resources and exits; read it with bmm_get_device_error()
+ * after synchronising the stream.
+ */
+#ifndef DMT_BMM_H
+#define DMT_BMM_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define BMM_API __attribute__((visibility("default")))
+#else
+#define BMM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element types (values of bmm_desc_t.typeA/typeB/typeC). */
+typedef enum {
+  BMM_BF16 = 0,
+  BMM_F16 = 1,
+  BMM_F32 = 2
+} bmm_dtype_t;
+
+typedef enum {
+  BMM_OK = 0,
+  BMM_ERR_INVALID_ARG = 1,    /* a size, stride, type or pointer argument is invalid */
+  BMM_ERR_UNSUPPORTED = 2,    /* valid but outside what this build supports */
+  BMM_ERR_MISALIGNED = 3,     /* a base pointer lacks the alignment the plan needs */
+  BMM_ERR_CUDA = 4,           /* a CUDA runtime or driver call failed */
+  BMM_ERR_DEVICE_TIMEOUT = 5, /* a kernel's bounded wait expired (see above) */
+  BMM_ERR_NO_DEVICE = 6       /* no usable sm_103 device is current */
+} bmm_status_t;
+
+/* Problem description.  All sizes and strides are in elements. */
+typedef struct {
+  int64_t batch, M, N, K;
+  int64_t lda, ldb, ldc;
+  int64_t strideA, strideB, strideC;
+  int32_t transA, transB;     /* 0 or 1 */
+  int32_t typeA, typeB, typeC; /* bmm_dtype_t: A,B in {BF16,F16} and equal; C in {F32,BF16} */
+} bmm_desc_t;
+
+/* What the planner chose for a problem (for tests, benchmarks and logs). */
+typedef struct {
+  int32_t tile_m, tile_n, tile_k; /* MMA-view tile (after any operand swap) */
+  int32_t stages;                 /* shared-memory ring depth */
+  int32_t swap_ab;                /* 1: computes C^T = op(B)^T op(A)^T (skinny M) */
+  int32_t pack_a, pack_b;         /* 1: operand staged through the workspace */
+  int32_t even_k;                 /* 1: K is a multiple of tile_k (no tail tile) */
+  int32_t tmem_cols;              /* Tensor Memory columns allocated per CTA */
+  int64_t tiles;                  /* output tiles over the whole batch */
+  int64_t smem_bytes;             /* dynamic shared memory per CTA */
+  int64_t stage_bytes;            /* bytes of one ring stage (A tile + B tile) */
+  int64_t workspace_bytes;        /* device workspace the plan owns */
+} bmm_plan_info_t;
+
+typedef struct bmm_plan_s* bmm_plan_t;
+
+/*
+ * Validate `desc` and plan the product: tile shape by shape class (including
+ * the swap to C^T for skinny M), ring depth from the shared-memory budget
+ * (stages x (A tile + B tile), "Optimize Triton Block Parameters", Step 2),
+ * and, per operand, whether TMA reads it in place or it is first copied into
+ * an aligned workspace (TMA needs 16-byte strides and bases; "FLA Triton ->
+ * Gluon porting", section 3, TMA).
+ *
+ * Needs a current CUDA device of compute capability 10.3: it queries the SM
+ * count and allocates the plan's device error word and workspace
+ * (cudaMalloc).  Arguments are validated before any CUDA call.
+ * On success *plan owns those allocations until bmm_destroy.
+ * Returns BMM_OK, BMM_ERR_INVALID_ARG (null pointer, negative size, ld less
+ * than the stored row length, bad type combination, overlapping C batches),
+ * BMM_ERR_UNSUPPORTED (dimension beyond 2^31-1), BMM_ERR_NO_DEVICE or
+ * BMM_ERR_CUDA.  On error *plan is set to NULL.
+ */
+BMM_API bmm_status_t bmm_create(const bmm_desc_t* desc, bmm_plan_t* plan);
+
+/*
+ * Planning only, on the host, for a GB300 (152 SMs, 227 KB shared memory
+ * per CTA): fills *info with what bmm_create would choose.  Makes no CUDA
+ * call.  Returns BMM_OK or BMM_ERR_INVALID_ARG / BMM_ERR_UNSUPPORTED as
+ * bmm_create would.
+ */
+BMM_API bmm_status_t bmm_plan_query(const bmm_desc_t* desc, bmm_plan_info_t* info);
+
+/* Copy the plan's choices into *info.  BMM_ERR_INVALID_ARG on null. */
+BMM_API bmm_status_t bmm_get_plan_info(bmm_plan_t plan, bmm_plan_info_t* info);
+
+/*
+ * Enqueue C = alpha*op(A)*op(B) + beta*C on `stream` (a cudaStream_t; NULL
+ * is the legacy default stream).  A, B, C are device pointers owned by the
+ * caller and laid out as `desc` said at bmm_create.  Operands that the plan
+ * reads in place by TMA must have 16-byte-aligned base pointers; otherwise
+ * BMM_ERR_MISALIGNED is returned and nothing is enqueued.  C needs only
+ * element alignment.  Returns BMM_OK once the work is enqueued,
+ * BMM_ERR_INVALID_ARG (null plan or pointer), or BMM_ERR_CUDA (launch
+ * failure).  Does not synchronise.
+ */
+BMM_API bmm_status_t bmm_run(bmm_plan_t plan, const void* A, const void* B, void* C,
+                     float alpha, float beta, void* stream);
+
+/*
+ * Read and clear the plan's device error word.  Call only after the stream
+ * used by bmm_run has been synchronised (this call does a blocking copy).
+ * Returns BMM_OK, BMM_ERR_DEVICE_TIMEOUT, or BMM_ERR_CUDA.  If `detail` is
+ * not NULL it receives the raw word (role and wait site, 0 when clean).
+ */
+BMM_API bmm_status_t bmm_get_device_error(bmm_plan_t plan, uint32_t* detail);
+
+/*
+ * Free the plan's device allocations and host state.  Calls cudaFree, which
+ * synchronises with the device; it does not otherwise wait on user streams.
+ * NULL is accepted.  Returns BMM_OK or BMM_ERR_CUDA.
+ */
+BMM_API bmm_status_t bmm_destroy(bmm_plan_t plan);
+
+/* Static, human-readable name of a status code. */
+BMM_API const char* bmm_status_string(bmm_status_t status);
+
+/* Library version as (major << 16) | minor. */
+BMM_API int32_t bmm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DMT_BMM_H */

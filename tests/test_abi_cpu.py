@@ -1,0 +1,140 @@
+"""The C ABI on the host, with no GPU: the library loads, exports every
+symbol ``include/bmm.h`` declares, validates arguments before touching the
+device, and plans each workload as intended.  No compute call is made."""
+import os
+import re
+
+import pytest
+
+from dense_matmul_tensor_gb300 import bmm as api
+from dense_matmul_tensor_gb300 import build
+from dense_matmul_tensor_gb300 import workloads as wl
+
+from bmm_harness import desc_for
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return api.load_library()
+
+
+def declared_symbols():
+    syms = set()
+    inc = os.path.join(ROOT, "include")
+    for f in os.listdir(inc):
+        if f.endswith(".h"):
+            text = open(os.path.join(inc, f)).read()
+            syms |= set(re.findall(r"BMM_API\s+[\w\s\*]+?\b(\w+)\s*\(", text))
+    return syms
+
+
+def test_every_declared_symbol_is_exported(lib):
+    syms = declared_symbols()
+    assert {"bmm_create", "bmm_run", "bmm_destroy"} <= syms
+    for s in syms:
+        assert hasattr(lib, s), f"{s} declared in include/ but not exported"
+    assert set(api.EXPORTED) <= syms
+
+
+def test_status_strings_and_version(lib):
+    for code, name in [(0, "BMM_OK"), (1, "BMM_ERR_INVALID_ARG"), (3, "BMM_ERR_MISALIGNED"),
+                       (5, "BMM_ERR_DEVICE_TIMEOUT")]:
+        assert api.bmm_status_string(code) == name
+    assert api.bmm_version() >= 1
+
+
+def _desc(**kw):
+    base = dict(batch=2, M=64, N=64, K=64, lda=64, ldb=64, ldc=64, strideA=4096, strideB=4096,
+                strideC=4096, transA=0, transB=0, typeA="bf16", typeC="f32")
+    base.update(kw)
+    return api.make_desc(**base)
+
+
+@pytest.mark.parametrize("bad", [
+    dict(M=-1), dict(K=-5), dict(lda=63), dict(ldb=10), dict(ldc=63),
+    dict(transA=2), dict(typeA="f32"), dict(typeC="f16"), dict(strideA=-8),
+    dict(strideC=100),                        # C batch items would overlap
+    dict(typeB=1),                            # A bf16, B fp16
+])
+def test_invalid_arguments_rejected_before_any_device_call(lib, bad):
+    d = _desc(**bad)
+    with pytest.raises(api.BmmError) as e:
+        api.bmm_create(d)
+    assert e.value.status == api.BMM_ERR_INVALID_ARG
+    with pytest.raises(api.BmmError) as e:
+        api.bmm_plan_query(d)
+    assert e.value.status == api.BMM_ERR_INVALID_ARG
+
+
+def test_null_arguments(lib):
+    import ctypes
+    assert lib.bmm_create(None, None) == api.BMM_ERR_INVALID_ARG
+    assert lib.bmm_run(None, None, None, None, 1.0, 0.0, None) == api.BMM_ERR_INVALID_ARG
+    assert lib.bmm_get_plan_info(None, None) == api.BMM_ERR_INVALID_ARG
+    assert lib.bmm_destroy(None) == api.BMM_OK
+    assert lib.bmm_get_device_error(None, None) == api.BMM_ERR_INVALID_ARG
+    p = ctypes.c_void_p(1)
+    assert lib.bmm_create(ctypes.byref(_desc(M=-3)), ctypes.byref(p)) == api.BMM_ERR_INVALID_ARG
+    assert p.value is None  # set to NULL on error
+
+
+def test_dimensions_beyond_int32_unsupported(lib):
+    d = _desc(K=2 ** 31, lda=2 ** 31, strideA=2 ** 37)
+    with pytest.raises(api.BmmError) as e:
+        api.bmm_plan_query(d)
+    assert e.value.status == api.BMM_ERR_UNSUPPORTED
+
+
+def test_create_without_a_gpu_reports_no_device(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    with pytest.raises(api.BmmError) as e:
+        api.bmm_create(_desc())
+    assert e.value.status == api.BMM_ERR_NO_DEVICE
+
+
+SMEM_LIMIT = 227 * 1024
+
+
+def _stage_bytes_formula(bm, bn, bk, esz=2):
+    # stages x (A tile + B tile): "Optimize Triton Block Parameters", Step 2
+    return (bm * bk + bk * bn) * esz
+
+
+@pytest.mark.parametrize("name", sorted(wl.WORKLOADS))
+def test_planner_on_workloads(lib, name):
+    p = wl.WORKLOADS[name]
+    info = api.bmm_plan_query(desc_for(p))
+    assert info.tile_m == 128 and info.tile_k == 64
+    assert info.smem_bytes <= SMEM_LIMIT
+    raw = _stage_bytes_formula(info.tile_m, info.tile_n, info.tile_k)
+    assert info.stage_bytes == -(-raw // 1024) * 1024
+    assert info.stages * info.stage_bytes <= SMEM_LIMIT
+    assert info.stages >= 4
+    assert info.tmem_cols >= 2 * info.tile_n and info.tmem_cols <= 512
+    assert info.even_k == (p.K % 64 == 0)
+    if p is wl.SKINNY:
+        assert info.swap_ab == 1 and info.tile_n == 16
+        assert info.tiles == p.batch * 2          # N=256 over two 128-row MMA tiles
+    if p is wl.GEMM_4096:
+        assert info.tile_n == 256 and info.tiles == 32 * 16 and info.stages == 4
+        assert info.workspace_bytes == 0
+    if p is wl.RAGGED:
+        # B stored K x N with ld 999 (not a multiple of 8): staged; A (ld 1000) read in place
+        assert info.pack_b == 1 and info.pack_a == 0
+        assert info.workspace_bytes >= p.batch * p.K * 1000 * 2
+    if p is wl.ATTN_PV:
+        assert info.tile_n == 128
+
+
+def test_planner_boundary_shapes(lib):
+    # the pages' boundary shapes and the K = 48 tail against a 64-wide K tile
+    for M in (17, 63, 129):
+        info = api.bmm_plan_query(_desc(M=M, N=96, K=48, lda=48, ldb=96, ldc=96,
+                                        strideA=M * 48, strideB=48 * 96, strideC=M * 96))
+        assert info.even_k == 0
+        assert info.tiles >= 1

@@ -1,0 +1,211 @@
+"""GPU parity: the tcgen05 path through the C ABI against the fp64 oracle,
+element by element, on seeded inputs.
+
+Tolerance per element: 1e-5*|alpha|*sum_k|a_ik||b_kj| + 1e-5*|beta*C_in|,
+plus 2^-8*|C_ref| when C is bf16 (one rounding of an 8-bit significand).
+Small-integer inputs are exact in fp32 and must match bit for bit.
+"""
+import itertools
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from dense_matmul_tensor_gb300 import bmm as api
+from dense_matmul_tensor_gb300 import workloads as wl
+
+from bmm_harness import check_full, check_sampled, run_gpu, sample_indices, decode_c
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    api.load_library()
+
+
+# ------------------------------------------------------------ small exact
+
+@pytest.mark.parametrize("transA,transB", list(itertools.product([False, True], repeat=2)))
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_small_integers_bitwise(transA, transB, dtype):
+    """|x| <= 4 and K <= 4096 keep every partial sum an integer below 2^24:
+    the fp32 result must equal the oracle exactly."""
+    p = wl.Problem(batch=2, M=200, N=136, K=448, transA=transA, transB=transB, type_ab=dtype,
+                   type_c="f32", seed=61)
+    na, nb, _ = p.storage_elems()
+    x = wl.Inputs(wl.small_ints16(na, 611, -4, 4, dtype), wl.small_ints16(nb, 612, -4, 4, dtype), None)
+    c, info = run_gpu(p, x)
+    check_full(p, x, c, exact=True)
+
+
+def test_small_workload_full():
+    p = wl.SMALL
+    x = wl.make_inputs(p)
+    c, info = run_gpu(p, x)
+    assert info.tile_n == 64 and info.swap_ab == 0 and info.even_k == 1
+    check_full(p, x, c)
+
+
+# ------------------------------------------------- sweep of shapes and flags
+
+SWEEP_DIMS = [1, 15, 16, 17, 63, 64, 65, 127, 128, 129, 255, 257]
+ALPHA_BETA = [(1.0, 0.0), (0.5, 1.0), (0.0, 1.0), (-2.0, 0.25)]
+
+
+def _sweep_cases(n=48, seed=7):
+    rng = np.random.default_rng(seed)
+    cases = []
+    for t in range(n):
+        M, N, K = (int(rng.choice(SWEEP_DIMS)) for _ in range(3))
+        batch = int(rng.choice([1, 3]))
+        tA, tB = bool(rng.integers(2)), bool(rng.integers(2))
+        dtype = ["bf16", "f16"][int(rng.integers(2))]
+        tc = ["f32", "bf16"][int(rng.integers(2))]
+        ab = ALPHA_BETA[int(rng.integers(4))]
+        cases.append((batch, M, N, K, tA, tB, dtype, tc, ab))
+    return cases
+
+
+@pytest.mark.parametrize("case", _sweep_cases(), ids=lambda c: "b{}_{}x{}x{}_t{}{}_{}_{}_{}".format(
+    c[0], c[1], c[2], c[3], int(c[4]), int(c[5]), c[6], c[7], c[8]))
+def test_sweep(case):
+    batch, M, N, K, tA, tB, dtype, tc, (alpha, beta) = case
+    p = wl.Problem(batch=batch, M=M, N=N, K=K, transA=tA, transB=tB, type_ab=dtype, type_c=tc,
+                   alpha=alpha, beta=beta, seed=100 + M + N + K)
+    x = wl.make_inputs(p)
+    c, _ = run_gpu(p, x)
+    check_full(p, x, c)
+
+
+@pytest.mark.parametrize("transA,transB", list(itertools.product([False, True], repeat=2)))
+@pytest.mark.parametrize("M,N,K", [(300, 520, 200), (129, 257, 48), (17, 300, 1000), (640, 24, 130)])
+def test_multi_tile_ragged(M, N, K, transA, transB):
+    """Several tiles in M and N and a ragged K tail (K % 64 != 0)."""
+    p = wl.Problem(batch=3, M=M, N=N, K=K, transA=transA, transB=transB, type_ab="bf16",
+                   type_c="f32", alpha=1.0, beta=0.0, dist_ab="normal", seed=71)
+    x = wl.make_inputs(p)
+    c, info = run_gpu(p, x)
+    check_full(p, x, c)
+
+
+def test_padded_and_unaligned_leading_dimensions():
+    """lda/ldb not multiples of 8 elements go through the staging copy; ldc
+    padding must stay untouched."""
+    p = wl.Problem(batch=2, M=150, N=99, K=77, transA=True, transB=False, type_ab="f16",
+                   type_c="f32", alpha=0.5, beta=1.0, lda=153, ldb=101, ldc=103, seed=81)
+    x = wl.make_inputs(p)
+    c, info = run_gpu(p, x)
+    assert info.pack_a == 1 and info.pack_b == 1
+    check_full(p, x, c)
+
+
+def test_padded_aligned_leading_dimensions():
+    p = wl.Problem(batch=2, M=130, N=260, K=100, transB=True, type_ab="bf16", type_c="bf16",
+                   lda=136, ldb=112, ldc=272, sA=136 * 130 + 8, seed=82)
+    x = wl.make_inputs(p)
+    c, info = run_gpu(p, x)
+    assert info.pack_a == 0 and info.pack_b == 0
+    check_full(p, x, c)
+
+
+@pytest.mark.parametrize("which", ["A", "B"])
+def test_batch_broadcast(which):
+    p = wl.Problem(batch=4, M=96, N=80, K=72, type_ab="bf16", type_c="f32",
+                   sA=0 if which == "A" else None, sB=0 if which == "B" else None, seed=83)
+    x = wl.make_inputs(p)
+    c, _ = run_gpu(p, x)
+    check_full(p, x, c)
+
+
+def test_beta_zero_does_not_read_nan_c():
+    p = wl.Problem(batch=2, M=100, N=100, K=100, seed=84)
+    x = wl.make_inputs(p)
+    c, _ = run_gpu(p, x, c_fill="nan")
+    assert np.all(np.isfinite(decode_c(c, p)))
+    check_full(p, x, c)
+
+
+@pytest.mark.parametrize("tc", ["f32", "bf16"])
+def test_alpha_zero_and_k_zero(tc):
+    p = wl.Problem(batch=2, M=33, N=65, K=40, type_c=tc, alpha=0.0, beta=-0.5, seed=85)
+    x = wl.make_inputs(p)
+    c, _ = run_gpu(p, x)
+    check_full(p, x, c)
+    p0 = wl.Problem(batch=2, M=33, N=65, K=0, type_c=tc, alpha=1.0, beta=2.0, seed=86)
+    x0 = wl.make_inputs(p0)
+    c0, _ = run_gpu(p0, x0)
+    check_full(p0, x0, c0)
+    pz = wl.Problem(batch=2, M=33, N=65, K=0, type_c=tc, alpha=1.0, beta=0.0, seed=87)
+    cz, _ = run_gpu(pz, wl.make_inputs(pz), c_fill="nan")
+    assert np.all(decode_c(cz, pz) == 0.0)
+
+
+def test_empty_problem_is_a_no_op():
+    p = wl.Problem(batch=3, M=0, N=16, K=16, seed=88)
+    c, _ = run_gpu(p, wl.make_inputs(p))
+    assert c.size == 0
+
+
+def test_misaligned_base_is_rejected():
+    p = wl.Problem(batch=1, M=64, N=64, K=64, seed=89)
+    x = wl.make_inputs(p)
+    c, _ = run_gpu(p, x, a_offset=1, expect_status=api.BMM_ERR_MISALIGNED)
+
+
+def test_repeated_runs_and_streams():
+    """Same plan, several runs on a side stream: identical bits each time."""
+    p = wl.Problem(batch=2, M=256, N=384, K=320, transB=True, type_c="f32", seed=90)
+    x = wl.make_inputs(p)
+    s = torch.cuda.Stream()
+    first, _ = run_gpu(p, x, stream=s)
+    for _ in range(2):
+        again, _ = run_gpu(p, x, stream=s)
+        assert np.array_equal(first, again)
+    check_full(p, x, first)
+
+
+# ------------------------------------------------------- full-size workloads
+
+def test_workload_gemm_4096():
+    p = wl.GEMM_4096
+    x = wl.make_inputs(p)
+    c, info = run_gpu(p, x, guard=8192)
+    assert info.tile_n == 256 and info.even_k == 1 and info.swap_ab == 0
+    check_sampled(p, x, c, sample_indices(p, 3000, 1))
+
+
+def test_workload_ragged():
+    p = wl.RAGGED
+    x = wl.make_inputs(p)
+    c, info = run_gpu(p, x)
+    assert info.even_k == 0 and info.pack_b == 1 and info.pack_a == 0
+    check_sampled(p, x, c, sample_indices(p, 4000, 2))
+
+
+def test_workload_skinny():
+    p = wl.SKINNY
+    x = wl.make_inputs(p)
+    c, info = run_gpu(p, x)
+    assert info.swap_ab == 1 and info.tile_n == 16
+    check_sampled(p, x, c, sample_indices(p, 4000, 3))
+
+
+def test_workload_attention_pair():
+    """S = alpha Q K^T (fp32 out), then O = P V with P = bf16(softmax(S)) made
+    by the oracle from its own S (never from the GPU's)."""
+    qk, pv = wl.ATTN_QK, wl.ATTN_PV
+    Q, Kt, V = wl.attention_qkv()
+    xs = wl.Inputs(Q.ravel(), Kt.ravel(), None)
+    s_host, info = run_gpu(qk, xs)
+    assert info.tile_n == 256
+    check_sampled(qk, xs, s_host, sample_indices(qk, 3000, 4))
+    P = oracle.attention_probs_bf16(Q, Kt, batch=128, L=2048, D=128, alpha=qk.alpha)
+    xo = wl.Inputs(P.ravel(), V.ravel(), None)
+    o_host, info = run_gpu(pv, xo)
+    assert info.tile_n == 128
+    check_sampled(pv, xo, o_host, sample_indices(pv, 3000, 5))
