@@ -136,11 +136,12 @@ def test_alpha_zero_and_k_zero(tc):
     x = wl.make_inputs(p)
     c, _ = run_gpu(p, x)
     check_full(p, x, c)
-    p0 = wl.Problem(batch=2, M=33, N=65, K=0, type_c=tc, alpha=1.0, beta=2.0, seed=86)
+    # K = 0: A is M x 0 and needs lda >= 1 (BLAS convention); C = beta * C
+    p0 = wl.Problem(batch=2, M=33, N=65, K=0, type_c=tc, alpha=1.0, beta=2.0, lda=8, seed=86)
     x0 = wl.make_inputs(p0)
     c0, _ = run_gpu(p0, x0)
     check_full(p0, x0, c0)
-    pz = wl.Problem(batch=2, M=33, N=65, K=0, type_c=tc, alpha=1.0, beta=0.0, seed=87)
+    pz = wl.Problem(batch=2, M=33, N=65, K=0, type_c=tc, alpha=1.0, beta=0.0, lda=8, seed=87)
     cz, _ = run_gpu(pz, wl.make_inputs(pz), c_fill="nan")
     assert np.all(decode_c(cz, pz) == 0.0)
 
