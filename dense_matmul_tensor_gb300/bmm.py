@@ -197,3 +197,24 @@ class Plan:
             self.close()
         except Exception:
             pass
+
+
+def bmm_run_noalloc(desc: bmm_desc_t, A, B, C, alpha=1.0, beta=0.0, stream=None,
+                    device_error=None) -> None:
+    """The allocation-free variant of bmm_run, for callers that cannot call
+    cudaMalloc (an allocator owns the device memory, or the call path cannot
+    afford cudaMalloc's cost and device synchronisation).  Plans ``desc`` for
+    this call and uses only the library's built-in device scratch (32 MiB of
+    operand staging plus an error word, shared by all calls: serialise calls
+    whose GPU work would overlap).  ``device_error`` is an optional device
+    pointer that receives the call's device error word on ``stream``."""
+    lib = load_library()
+    fn = lib.bmm_run_noalloc
+    if fn.argtypes is None:
+        vp = ctypes.c_void_p
+        fn.argtypes = [ctypes.POINTER(bmm_desc_t), vp, vp, vp, ctypes.c_float, ctypes.c_float, vp, vp]
+        fn.restype = ctypes.c_int
+    st = fn(ctypes.byref(desc), _ptr(A), _ptr(B), _ptr(C), float(alpha), float(beta),
+            _stream(stream), _ptr(device_error))
+    if st != BMM_OK:
+        raise BmmError(st, "bmm_run_noalloc")

@@ -440,3 +440,84 @@ bmm_status_t bmm_destroy(bmm_plan_t pl) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of bmm_run.
+//
+// Some callers cannot call cudaMalloc: code that runs under an allocator that
+// owns the device's memory (a framework's caching pool, a fixed memory budget
+// carved out up front), and latency-critical call paths where cudaMalloc's
+// cost and its implicit device synchronisation are not acceptable.  For them,
+// bmm_run_noalloc takes the problem description directly and keeps all of its
+// scratch (the device error word and the staging area for operands whose
+// strides TMA cannot read in place) in one file-scope device array.  That
+// array is part of the library image: every GPU that loads the library holds
+// it until the process exits.
+namespace {
+
+constexpr size_t kNoAllocWordBytes = 256;             // device error word region
+constexpr size_t kNoAllocStagingMax = size_t(32) << 20;  // 32 MiB operand staging area
+constexpr int kNoAllocMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocWordBytes + kNoAllocStagingMax];
+
+std::mutex g_noalloc_mu;
+unsigned char* g_noalloc_addr[kNoAllocMaxDevices];
+
+// Device address of the scratch array on device `dev` (which must be
+// current).  Looked up with cudaGetSymbolAddress on the first call per device.
+bmm_status_t noalloc_scratch(int dev, unsigned char** out) {
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return BMM_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+      return BMM_ERR_CUDA;
+    g_noalloc_addr[dev] = static_cast<unsigned char*>(p);
+  }
+  *out = g_noalloc_addr[dev];
+  return BMM_OK;
+}
+
+}  // namespace
+
+extern "C" bmm_status_t bmm_run_noalloc(const bmm_desc_t* desc, const void* A, const void* B,
+                                        void* C, float alpha, float beta, void* stream,
+                                        uint32_t* device_error) {
+  const bmm_status_t st = validate(desc);
+  if (st != BMM_OK) return st;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return BMM_ERR_NO_DEVICE;
+  int major = 0, minor = 0, sms = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return BMM_ERR_NO_DEVICE;
+  if (major != 10 || minor != 3) return BMM_ERR_NO_DEVICE;
+  if (!get_encoder()) return BMM_ERR_CUDA;
+
+  bmm_plan_s pl;  // on the stack: nothing is allocated for the call
+  std::memset(static_cast<void*>(&pl), 0, sizeof(pl));
+  pl.d = *desc;
+  plan(desc, &pl.P);
+  if (pl.P.workspace_bytes > static_cast<int64_t>(kNoAllocStagingMax)) return BMM_ERR_UNSUPPORTED;
+  unsigned char* scratch = nullptr;
+  const bmm_status_t sst = noalloc_scratch(dev, &scratch);
+  if (sst != BMM_OK) return sst;
+  pl.device = dev;
+  pl.sms = sms;
+  pl.timeout_ns = wait_timeout_ns();
+  pl.err = reinterpret_cast<uint32_t*>(scratch);
+  pl.ws = scratch + kNoAllocWordBytes;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // The array keeps the previous call's contents: the error word must start at zero.
+  if (cudaMemsetAsync(pl.err, 0, sizeof(uint32_t), s) != cudaSuccess) return BMM_ERR_CUDA;
+  const bmm_status_t rst = bmm_run(&pl, A, B, C, alpha, beta, stream);
+  if (rst != BMM_OK) return rst;
+  if (device_error &&
+      cudaMemcpyAsync(device_error, pl.err, sizeof(uint32_t), cudaMemcpyDeviceToDevice, s) !=
+          cudaSuccess)
+    return BMM_ERR_CUDA;
+  return BMM_OK;
+}

@@ -163,6 +163,38 @@ BMM_API bmm_status_t bmm_get_device_error(bmm_plan_t plan, uint32_t* detail);
  */
 BMM_API bmm_status_t bmm_destroy(bmm_plan_t plan);
 
+/*
+ * bmm_run without any allocation, for callers that cannot call cudaMalloc:
+ * code running under an allocator that owns the device's memory (a caching
+ * pool, a fixed budget reserved up front) and latency-critical call paths
+ * that cannot afford cudaMalloc's cost and implicit device synchronisation.
+ * The pages have no counterpart to this entry point.
+ *
+ * It plans `desc` on the host for this call and enqueues the same kernels as
+ * bmm_run on `stream`.  Its only scratch is one device array inside the
+ * library (every GPU that loads the library holds it until exit): a 256-byte
+ * error-word region plus a 32 MiB staging area for operands whose strides or
+ * batch strides are not multiples of 16 bytes.  A problem that would need
+ * more staging than 32 MiB is rejected with BMM_ERR_UNSUPPORTED before
+ * anything is enqueued.  It calls no cudaMalloc, cudaFree or allocating
+ * library routine.
+ *
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  Every call shares the array and it keeps the
+ * last call's contents, so calls whose work overlaps on the GPU (other
+ * streams, other host threads) race on it: serialise them.  The error word
+ * is cleared on `stream` at the start of each call.  If `device_error` is a
+ * device pointer (not NULL), the call also copies the word there on
+ * `stream`: 0, or the BMM_ERR_DEVICE_TIMEOUT detail described for
+ * bmm_get_device_error, once the stream reaches it.
+ *
+ * Pointers, alignment and return codes are as for bmm_create + bmm_run.
+ */
+BMM_API bmm_status_t bmm_run_noalloc(const bmm_desc_t* desc, const void* A, const void* B,
+                                     void* C, float alpha, float beta, void* stream,
+                                     uint32_t* device_error);
+
 /* Static, human-readable name of a status code. */
 BMM_API const char* bmm_status_string(bmm_status_t status);
 
