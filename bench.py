@@ -332,6 +332,23 @@ class OracleSample:
 
 # ------------------------------------------------------------------ main
 
+def reduce_max(x: float, world: int, device=None) -> float:
+    """Max of ``x`` over all ranks (the slowest rank sets the job's time)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_rank: float, world: int, ms_slowest: float) -> float:
+    """Weak scaling: every rank does ``flops_per_rank``; the job takes as long
+    as its slowest rank."""
+    return world * flops_per_rank / (ms_slowest * 1e-3) / 1e12
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -390,11 +407,7 @@ def main():
             dist.barrier()
 
     def max_over_ranks(x):
-        if world == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return reduce_max(x, world, dev)
 
     peaks, peak_src = load_peaks()
     stream = torch.cuda.Stream(device=dev)
@@ -409,13 +422,15 @@ def main():
     clocks.stop()
     ms_mean = statistics.fmean(ms_list)
     ms_step = max_over_ranks(ms_mean)
-    value = world * p.flops() / (ms_step * 1e-3) / 1e12
+    value = whole_job_tflops(p.flops(), world, ms_step)
 
     achieved = p.flops() / (ms_mean * 1e-3) / 1e12
     roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
             "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
             "traffic": NCU_TRAFFIC.get(kernel_source_hash()),
-            "kernel": f"bmm_tc_kernel<{info.tile_n}>", "peak_source": f"{peak_src} bf16 burst",
+            "kernel": (f"bmm_tc2_kernel<{info.tile_n}> (CTA pairs)" if info.cta_pair
+                       else f"bmm_tc_kernel<{info.tile_n}>"),
+            "peak_source": f"{peak_src} bf16 burst",
             "algorithmic_flops_per_launch": p.flops(),
             "ms_per_launch_median": statistics.median(ms_list),
             "achieved_median": p.flops() / (statistics.median(ms_list) * 1e-3) / 1e12}
@@ -429,6 +444,7 @@ def main():
                        "output": p.type_c, "alpha": p.alpha, "beta": p.beta,
                        "l2": f"flushed: {FLUSH_BYTES >> 20} MB write between timed steps",
                        "tile": [info.tile_m, info.tile_n, info.tile_k], "stages": info.stages,
+                       "cta_pair": bool(info.cta_pair),
                        "parallelism": f"{world} independent replicas" if world > 1 else "1 GPU"},
             "roofline": roof,
             "gpu_launches": launches * args.steps,
@@ -438,7 +454,7 @@ def main():
         e2e_steps = max(5, min(args.steps, 50))
         ms_e, h2d, d2h = time_e2e(p, e2e_steps, 3, stream, dev)
         ms_e = max_over_ranks(ms_e)
-        line["e2e"] = {"value": world * p.flops() / (ms_e * 1e-3) / 1e12, "unit": "TFLOP/s",
+        line["e2e"] = {"value": whole_job_tflops(p.flops(), world, ms_e), "unit": "TFLOP/s",
                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                        "ms_per_step": ms_e}
 
@@ -459,6 +475,7 @@ def main():
                           "frac_hbm": gbs / peaks["hbm_gbs"],
                           "intensity_flop_per_byte": q.flops() / q.algorithmic_bytes(),
                           "tile_n": qinfo.tile_n, "swap_ab": qinfo.swap_ab,
+                          "cta_pair": qinfo.cta_pair,
                           "pack": [qinfo.pack_a, qinfo.pack_b]})
             del qa, qb, qc
             torch.cuda.empty_cache()

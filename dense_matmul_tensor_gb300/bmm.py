@@ -37,7 +37,7 @@ class bmm_desc_t(ctypes.Structure):
 class bmm_plan_info_t(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in
                 ("tile_m", "tile_n", "tile_k", "stages", "swap_ab", "pack_a", "pack_b", "even_k",
-                 "tmem_cols")] + \
+                 "tmem_cols", "cta_pair")] + \
                [(n, ctypes.c_int64) for n in
                 ("tiles", "smem_bytes", "stage_bytes", "workspace_bytes")]
 

@@ -36,6 +36,7 @@ struct Operand {
 
 struct Planned {
   int swap;
+  int pair;          // 1: CTA pairs (2-SM MMA, 256-row tiles)
   int64_t batch, Mv, Nv, K;
   Operand a, b;
   int bn, stages;
@@ -68,8 +69,31 @@ bmm_status_t validate(const bmm_desc_t* d) {
   return BMM_OK;
 }
 
-// Shape classes and resources.  Pure host arithmetic (no CUDA calls).
-void plan(const bmm_desc_t* d, Planned* P) {
+// Tile N for the large class, chosen to balance waves: the persistent grid
+// runs ceil(tiles / units) rounds of tiles whose cost grows with N, so the
+// estimate rounds x N is minimised over the tile widths the operand layout
+// allows (a 4096-wide problem on 76 CTA pairs: 256 -> 4 rounds of 256,
+// 224 -> 4 rounds of 224, so 224).  Ties keep the wider tile.
+int balanced_tile_n(int64_t batch, int64_t Mv, int64_t Nv, int tile_m, int64_t units,
+                    const int* cands, int ncand) {
+  int best = cands[0];
+  int64_t best_cost = -1;
+  for (int i = 0; i < ncand; ++i) {
+    const int bn = cands[i];
+    const int64_t tiles = batch * ((Mv + tile_m - 1) / tile_m) * ((Nv + bn - 1) / bn);
+    const int64_t rounds = (tiles + units - 1) / units;
+    const int64_t cost = rounds * bn;
+    if (best_cost < 0 || cost < best_cost) {
+      best = bn;
+      best_cost = cost;
+    }
+  }
+  return best;
+}
+
+// Shape classes and resources.  Pure host arithmetic (no CUDA calls); `sms`
+// is the device's SM count (152 on GB300).
+void plan(const bmm_desc_t* d, Planned* P, int sms) {
   std::memset(P, 0, sizeof(*P));
   // Skinny M: compute C^T = op(B)^T op(A)^T so that N fills the 128-row MMA.
   P->swap = (d->M <= 64 && d->N > d->M) ? 1 : 0;
@@ -108,9 +132,37 @@ void plan(const bmm_desc_t* d, Planned* P) {
   else if (P->Nv <= 32 && !P->b.mn_major) bn = 32;
   else if (P->Nv <= 64) bn = 64;
   else if (P->Nv <= 128) bn = 128;
+  // Large tiles run on CTA pairs (tcgen05 cta_group::2, 256 rows per pair):
+  // each SM then takes in a third less operand data per FLOP.  The
+  // environment variable DMT_BMM_PAIR=0 keeps the 1-CTA kernel (comparisons).
+  const char* pe = std::getenv("DMT_BMM_PAIR");
+  const bool pair_off = pe && pe[0] == '0';
+  P->pair = (bn == 256 && P->Mv > dmt::kTileM && !pair_off) ? 1 : 0;
+  const int tile_m = P->pair ? 2 * dmt::kTileM : dmt::kTileM;
+  if (bn == 256) {
+    // K-major B tiles may be any multiple of 16 rows; MN-major B tiles are
+    // loaded in 64-column boxes (per CTA of a pair: BN/2 columns).
+    static const int kK[3] = {256, 224, 192};
+    static const int kMnSingle[2] = {256, 192};
+    const int units = P->pair ? sms / 2 : sms;
+    if (!P->b.mn_major)
+      bn = balanced_tile_n(P->batch, P->Mv, P->Nv, tile_m, units > 0 ? units : 1, kK, 3);
+    else if (!P->pair)
+      bn = balanced_tile_n(P->batch, P->Mv, P->Nv, tile_m, units > 0 ? units : 1, kMnSingle, 2);
+    // DMT_BMM_TILE_N pins one of the widths this layout allows (comparisons).
+    const char* te = std::getenv("DMT_BMM_TILE_N");
+    if (te && *te) {
+      const int want = std::atoi(te);
+      const int* c = !P->b.mn_major ? kK : (P->pair ? kK : kMnSingle);
+      const int n = !P->b.mn_major ? 3 : (P->pair ? 1 : 2);
+      for (int i = 0; i < n; ++i)
+        if (c[i] == want) bn = want;
+    }
+  }
   P->bn = bn;
+  const int b_rows = P->pair ? bn / 2 : bn;  // B tile rows held by one CTA
   P->a.box_rows = dmt::kTileM;
-  P->b.box_rows = bn;
+  P->b.box_rows = b_rows;
 
   // TMA needs 16-byte row and batch strides; otherwise stage a copy with
   // ld rounded up to 8 elements.
@@ -131,7 +183,7 @@ void plan(const bmm_desc_t* d, Planned* P) {
   P->workspace_bytes = ws;
 
   P->a_bytes = static_cast<uint32_t>(dmt::kTileM * dmt::kTileK * 2);
-  const uint32_t b_bytes = static_cast<uint32_t>(bn * dmt::kTileK * 2);
+  const uint32_t b_bytes = static_cast<uint32_t>(b_rows * dmt::kTileK * 2);
   P->stage_bytes = static_cast<uint32_t>(round_up(P->a_bytes + b_bytes, 1024));
   P->tx_bytes = P->a_bytes + b_bytes;
   const int64_t fixed = 1024 + dmt::kEpiBytes + dmt::kBarBytes;
@@ -150,9 +202,9 @@ void plan(const bmm_desc_t* d, Planned* P) {
              | (static_cast<uint32_t>(P->a.mn_major) << 15) |
              (static_cast<uint32_t>(P->b.mn_major) << 16) |
              (static_cast<uint32_t>(bn >> 3) << 17)      // N / 8
-             | (static_cast<uint32_t>(dmt::kTileM >> 4) << 24);  // M / 16
+             | (static_cast<uint32_t>(tile_m >> 4) << 24);  // M / 16
 
-  P->num_m = static_cast<int32_t>((P->Mv + dmt::kTileM - 1) / dmt::kTileM);
+  P->num_m = static_cast<int32_t>((P->Mv + tile_m - 1) / tile_m);
   P->num_n = static_cast<int32_t>((P->Nv + bn - 1) / bn);
   P->tiles = P->batch * P->num_m * P->num_n;
   P->k_blocks = static_cast<int32_t>((P->K + dmt::kTileK - 1) / dmt::kTileK);
@@ -163,7 +215,7 @@ void plan(const bmm_desc_t* d, Planned* P) {
 
 void fill_info(const Planned& P, const bmm_desc_t* d, bmm_plan_info_t* info) {
   std::memset(info, 0, sizeof(*info));
-  info->tile_m = dmt::kTileM;
+  info->tile_m = P.pair ? 2 * dmt::kTileM : dmt::kTileM;
   info->tile_n = P.bn;
   info->tile_k = dmt::kTileK;
   info->stages = P.stages;
@@ -172,6 +224,7 @@ void fill_info(const Planned& P, const bmm_desc_t* d, bmm_plan_info_t* info) {
   info->pack_b = P.swap ? P.a.pack : P.b.pack;
   info->even_k = (d->K % dmt::kTileK) == 0 ? 1 : 0;
   info->tmem_cols = static_cast<int32_t>(P.tmem_cols);
+  info->cta_pair = P.pair;
   info->tiles = P.tiles;
   info->smem_bytes = P.smem_bytes;
   info->stage_bytes = P.stage_bytes;
@@ -205,6 +258,17 @@ bool prepare_kernel(int64_t smem) {
   return ok;
 }
 
+template <int BN>
+bool prepare_pair_kernel() {
+  static std::once_flag once;
+  static bool ok = false;
+  std::call_once(once, [] {
+    ok = cudaFuncSetAttribute(dmt::bmm_tc2_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(dmt::kSmemLimit)) == cudaSuccess;
+  });
+  return ok;
+}
+
 uint64_t wait_timeout_ns() {
   const char* e = std::getenv("DMT_BMM_WAIT_TIMEOUT_MS");
   if (e && *e) {
@@ -221,11 +285,13 @@ struct bmm_plan_s {
   Planned P;
   int device;
   int sms;
+  int max_pairs;  // co-resident CTA pairs for the pair kernel (0: not queried)
   void* ws;
   uint32_t* err;
   uint64_t timeout_ns;
-  const void* map_ptr[2];
-  CUtensorMap map[2];
+  int test_stall;
+  const void* map_ptr[3];
+  CUtensorMap map[3];  // A, B, and C (C only when written by TMA box stores)
 };
 
 namespace {
@@ -249,13 +315,67 @@ bool encode_map(const bmm_plan_s* pl, const Operand& o, const void* base, CUtens
   return r == CUDA_SUCCESS;
 }
 
+cudaLaunchConfig_t pair_config(int64_t pairs, int64_t smem, cudaStream_t stream,
+                               cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs), 1, 1);
+  cfg.blockDim = dim3(dmt::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = stream;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
+// Persistent grid of CTA pairs: as many as can be co-resident (queried once
+// per plan), at most one per pair tile.
+template <int BN>
+cudaError_t launch_gemm_pair(bmm_plan_s* pl, const KParams& kp, cudaStream_t stream) {
+  if (!prepare_pair_kernel<BN>()) return cudaErrorInvalidValue;
+  cudaLaunchAttribute attr[1];
+  if (pl->max_pairs == 0) {
+    cudaLaunchConfig_t q = pair_config(pl->sms / 2, pl->P.smem_bytes, stream, attr);
+    int n = 0;
+    const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, dmt::bmm_tc2_kernel<BN>, &q);
+    if (e != cudaSuccess) return e;
+    pl->max_pairs = n > 0 ? n : 1;
+  }
+  const int64_t pairs = pl->P.tiles < pl->max_pairs ? pl->P.tiles : pl->max_pairs;
+  cudaLaunchConfig_t cfg = pair_config(pairs, pl->P.smem_bytes, stream, attr);
+  return cudaLaunchKernelEx(&cfg, dmt::bmm_tc2_kernel<BN>, kp, pl->map[0], pl->map[1], pl->map[2]);
+}
+
+// C as a 3-D tensor (N, M, batch) with 32 x 32 boxes: 128-byte box rows for
+// fp32 (128-byte swizzle), 64-byte rows for bf16 (64-byte swizzle), matching
+// the layout the epilogue writes into its box buffers.
+bool encode_c_map(const bmm_plan_s* pl, void* C, CUtensorMap* out) {
+  const bmm_desc_t& d = pl->d;
+  const int64_t es = d.typeC == BMM_F32 ? 4 : 2;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d.N), static_cast<cuuint64_t>(d.M),
+                        static_cast<cuuint64_t>(d.batch)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d.ldc * es),
+                           static_cast<cuuint64_t>(d.batch > 1 ? d.strideC * es
+                                                               : round_up(d.M * d.ldc * es, 16))};
+  cuuint32_t box[3] = {32u, 32u, 1u};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  const CUresult r = g_encode(out, es == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                              3, C, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              es == 4 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 template <int BN>
 cudaError_t launch_gemm(const bmm_plan_s* pl, const KParams& kp, cudaStream_t stream) {
   if (!prepare_kernel<BN>(pl->P.smem_bytes)) return cudaErrorInvalidValue;
   int64_t grid = pl->P.tiles < pl->sms ? pl->P.tiles : pl->sms;
   dmt::bmm_tc_kernel<BN><<<static_cast<unsigned>(grid), dmt::kThreads,
                            static_cast<size_t>(pl->P.smem_bytes), stream>>>(kp, pl->map[0],
-                                                                           pl->map[1]);
+                                                                           pl->map[1], pl->map[2]);
   return cudaGetLastError();
 }
 
@@ -283,7 +403,7 @@ bmm_status_t bmm_plan_query(const bmm_desc_t* desc, bmm_plan_info_t* info) {
   const bmm_status_t st = validate(desc);
   if (st != BMM_OK) return st;
   Planned P;
-  plan(desc, &P);
+  plan(desc, &P, kGb300Sms);
   fill_info(P, desc, info);
   (void)kGb300Sms;
   return BMM_OK;
@@ -308,10 +428,14 @@ bmm_status_t bmm_create(const bmm_desc_t* desc, bmm_plan_t* out) {
   bmm_plan_s* pl = new (std::nothrow) bmm_plan_s();
   if (!pl) return BMM_ERR_CUDA;
   pl->d = *desc;
-  plan(desc, &pl->P);
+  plan(desc, &pl->P, sms);
   pl->device = dev;
   pl->sms = sms;
   pl->timeout_ns = wait_timeout_ns();
+  // Test hook for failure detection: the MMA thread waits on a barrier that
+  // nothing completes, so its bounded wait must expire (see bmm.h, errors).
+  const char* ts = std::getenv("DMT_BMM_TEST_STALL_MMA");
+  pl->test_stall = (ts && ts[0] == '1') ? 1 : 0;
   if (cudaMalloc(reinterpret_cast<void**>(&pl->err), 256) != cudaSuccess ||
       cudaMemset(pl->err, 0, 256) != cudaSuccess) {
     cudaFree(pl->err);
@@ -362,9 +486,9 @@ bmm_status_t bmm_run(bmm_plan_t pl, const void* A, const void* B, void* C, float
     if (o.pack) {
       uint16_t* dst = reinterpret_cast<uint16_t*>(static_cast<char*>(pl->ws) + o.ws_off);
       const int64_t nb = o.bcast ? 1 : d.batch;
-      const int64_t rows = nb * o.rows;
-      dim3 grid(static_cast<unsigned>((o.cols + 255) / 256 < 64 ? (o.cols + 255) / 256 : 64),
-                static_cast<unsigned>(rows < 65535 ? rows : 65535));
+      const int64_t segs = nb * o.rows * ((o.cols + 7) / 8);
+      const int64_t blocks = (segs + 255) / 256;
+      const unsigned grid = static_cast<unsigned>(blocks < 8 * pl->sms ? blocks : 8 * pl->sms);
       dmt::pack16_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(src), dst, nb,
                                                    o.rows, o.cols, o.ld, o.bcast ? 0 : o.stride,
                                                    o.pld, o.pstride);
@@ -405,17 +529,42 @@ bmm_status_t bmm_run(bmm_plan_t pl, const void* A, const void* B, void* C, float
   kp.sC = d.strideC;
   kp.c_bf16 = d.typeC == BMM_BF16 ? 1 : 0;
   kp.c_trans = P.swap;
+  // Row-major C with beta == 0 goes out through TMA box stores when its base,
+  // strides and row length are 16-byte multiples (a box store writes whole
+  // 16-byte chunks at the row end, which would spill past a ragged row);
+  // otherwise coalesced direct stores.
+  {
+    const int64_t es = d.typeC == BMM_F32 ? 4 : 2;
+    const bool aligned = (reinterpret_cast<uintptr_t>(C) & 15u) == 0 && (d.ldc * es) % 16 == 0 &&
+                         (d.N * es) % 16 == 0 && (d.batch <= 1 || (d.strideC * es) % 16 == 0);
+    kp.c_tma = (!P.swap && beta == 0.0f && aligned && P.bn >= 32) ? 1 : 0;
+    if (kp.c_tma && pl->map_ptr[2] != C) {
+      if (!encode_c_map(pl, C, &pl->map[2])) return BMM_ERR_CUDA;
+      pl->map_ptr[2] = C;
+    }
+  }
   kp.alpha = alpha;
   kp.beta = beta;
   kp.err = pl->err;
   kp.timeout_ns = pl->timeout_ns;
+  kp.test_stall = pl->test_stall;
 
   cudaError_t e;
+  if (P.pair) {
+    switch (P.bn) {
+      case 192: e = launch_gemm_pair<192>(pl, kp, stream); break;
+      case 224: e = launch_gemm_pair<224>(pl, kp, stream); break;
+      default: e = launch_gemm_pair<256>(pl, kp, stream); break;
+    }
+    return e == cudaSuccess ? BMM_OK : BMM_ERR_CUDA;
+  }
   switch (P.bn) {
     case 16: e = launch_gemm<16>(pl, kp, stream); break;
     case 32: e = launch_gemm<32>(pl, kp, stream); break;
     case 64: e = launch_gemm<64>(pl, kp, stream); break;
     case 128: e = launch_gemm<128>(pl, kp, stream); break;
+    case 192: e = launch_gemm<192>(pl, kp, stream); break;
+    case 224: e = launch_gemm<224>(pl, kp, stream); break;
     default: e = launch_gemm<256>(pl, kp, stream); break;
   }
   return e == cudaSuccess ? BMM_OK : BMM_ERR_CUDA;
@@ -499,7 +648,7 @@ extern "C" bmm_status_t bmm_run_noalloc(const bmm_desc_t* desc, const void* A, c
   bmm_plan_s pl;  // on the stack: nothing is allocated for the call
   std::memset(static_cast<void*>(&pl), 0, sizeof(pl));
   pl.d = *desc;
-  plan(desc, &pl.P);
+  plan(desc, &pl.P, sms);
   if (pl.P.workspace_bytes > static_cast<int64_t>(kNoAllocStagingMax)) return BMM_ERR_UNSUPPORTED;
   unsigned char* scratch = nullptr;
   const bmm_status_t sst = noalloc_scratch(dev, &scratch);

@@ -49,7 +49,11 @@ constexpr int kUmmaK = 16;    // K of one tcgen05.mma kind::f16
 constexpr int kThreads = 192; // producer, MMA, 4 epilogue warps
 constexpr int kGroupM = 8;
 constexpr int kEpiPitch = 33; // floats per staged row (bank-conflict-free)
-constexpr uint32_t kEpiBytes = 4u * 32u * kEpiPitch * 4u;
+// Epilogue staging, shared by the two store paths: four 32 x 33 fp32 tiles
+// (coalesced direct stores) or two 4 KB TMA-store boxes per epilogue warp.
+constexpr uint32_t kEpiBoxBytes = 4096u;
+constexpr uint32_t kEpiBytes = 4u * 2u * kEpiBoxBytes;
+static_assert(kEpiBytes >= 4u * 32u * kEpiPitch * 4u, "direct-store staging must fit");
 constexpr uint32_t kBarBytes = 512;   // barriers, TMEM slot, abort flag
 constexpr uint32_t kSmemLimit = 232448;  // 227 KB dynamic shared memory per CTA
 
@@ -60,6 +64,7 @@ enum WaitSite : uint32_t {
   kSiteMmaAccEmpty = 2,
   kSiteMmaFull = 3,
   kSiteEpiAccFull = 4,
+  kSiteTestStall = 5,
 };
 
 struct KParams {
@@ -80,9 +85,11 @@ struct KParams {
   int64_t ldc, sC;         // C strides (elements), user layout
   int32_t c_bf16;          // C element type: 1 = bf16, 0 = fp32
   int32_t c_trans;         // 1: D = C^T (operands swapped): D(i, j) -> C[j*ldc + i]
+  int32_t c_tma;           // 1: row-major C written with TMA box stores (tensor map tmC)
   float alpha, beta;
   uint32_t* err;           // device error word
   uint64_t timeout_ns;     // bound on any single wait
+  int32_t test_stall;      // 1: the MMA thread first waits on a barrier nothing completes
 };
 
 struct Abort {
@@ -91,13 +98,21 @@ struct Abort {
   uint64_t timeout_ns;
 };
 
+template <bool kSpin>
+__device__ __forceinline__ bool mbar_probe(uint32_t bar, uint32_t parity) {
+  return kSpin ? mbar_try_wait_spin(bar, parity) : mbar_try_wait(bar, parity);
+}
+
 // Slow path of a bounded wait: poll until the phase completes, another role
-// raises the abort flag, or the time limit passes (then raise it).
+// raises the abort flag, or the time limit passes (then raise it).  kSpin
+// polls without parking the thread (producer and MMA threads, whose wake-up
+// latency sits on the pipeline's critical path).
+template <bool kSpin>
 __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, Abort ab, uint32_t site) {
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1; it < (1u << 30); ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 15u) == 0) {
+    if (mbar_probe<kSpin>(bar, parity)) return true;
+    if ((it & (kSpin ? 63u : 15u)) == 0) {
       if (*ab.flag) return false;
       if (global_timer_ns() - t0 > ab.timeout_ns) break;
     }
@@ -107,13 +122,15 @@ __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, Abort ab, 
   return false;
 }
 
+template <bool kSpin = false>
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, Abort ab, uint32_t site) {
-  if (mbar_try_wait(bar, parity)) return true;
-  return wait_slow(bar, parity, ab, site);
+  if (mbar_probe<kSpin>(bar, parity)) return true;
+  return wait_slow<kSpin>(bar, parity, ab, site);
 }
 
-// Wait with a short fixed limit and no error report: used only on the abort
-// path to let this CTA's own asynchronous copies and MMAs land before exit.
+// Wait with a short fixed limit and no error report: before exit, lets this
+// CTA's own asynchronous copies and MMAs land (at once after a normal run;
+// bounded after an abort).
 __device__ __noinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 0; it < (1u << 24); ++it) {
@@ -148,50 +165,119 @@ __device__ __forceinline__ void store_c(const KParams& p, int64_t off, float v) 
 }
 
 // One chunk of CW accumulator columns held by this thread (row `lane` of the
-// warp's 32-lane quarter) -> C.
+// warp's 32-lane quarter) -> C with coalesced direct stores (any alignment,
+// beta != 0, or the swapped C^T form).  Rows go in groups of eight: the
+// group's loads are all issued before its first store (C may alias nothing
+// the compiler can prove, so interleaving would serialise one memory latency
+// per row), while the live registers stay bounded.
 template <int CW>
 __device__ __forceinline__ void store_chunk(const KParams& p, float (&v)[CW], float* stg, int lane,
                                             int row0, int col0, int64_t cbase) {
+  constexpr int G = 8;
   const float alpha = p.alpha, beta = p.beta;
+#pragma unroll
+  for (int r = 0; r < CW; ++r) v[r] *= alpha;
   if (p.c_trans) {
     // D row i = C column, D column j = C row: lanes write consecutive C columns.
     const int i = row0 + lane;
     if (i < p.Mv) {
+      const int ncols = min(CW, p.Nv - col0);
+      int64_t off = cbase + static_cast<int64_t>(col0) * p.ldc + i;
 #pragma unroll
-      for (int r = 0; r < CW; ++r) {
-        const int j = col0 + r;
-        if (j < p.Nv) {
-          const int64_t off = cbase + static_cast<int64_t>(j) * p.ldc + i;
-          float out = alpha * v[r];
-          if (beta != 0.0f) out = fmaf(beta, load_c(p, off), out);
-          store_c(p, off, out);
+      for (int g = 0; g < CW; g += G) {
+        if (beta != 0.0f) {
+          float cin[G];
+          int64_t o = off;
+#pragma unroll
+          for (int r = 0; r < G; ++r, o += p.ldc)
+            if (g + r < ncols) cin[r] = load_c(p, o);
+#pragma unroll
+          for (int r = 0; r < G; ++r) v[g + r] = fmaf(beta, cin[r], v[g + r]);
         }
+#pragma unroll
+        for (int r = 0; r < G; ++r, off += p.ldc)
+          if (g + r < ncols) store_c(p, off, v[g + r]);
       }
     }
     return;
   }
-  // Row-major C: stage the 32 x CW block (thread = row) and write it back
-  // row by row (lane = column), so each warp store covers one C row.
+  // Row-major C: stage the 32 x CW block (thread = row) and read it back
+  // transposed (lane = column), so each warp store covers one C row.
 #pragma unroll
   for (int r = 0; r < CW; ++r) stg[lane * kEpiPitch + r] = v[r];
   __syncwarp();
   const int j = col0 + lane;
-  if (lane < CW && j < p.Nv) {
-    const int rows = min(32, p.Mv - row0);
-    for (int rr = 0; rr < rows; ++rr) {
-      const int64_t off = cbase + static_cast<int64_t>(row0 + rr) * p.ldc + j;
-      float out = alpha * stg[rr * kEpiPitch + lane];
-      if (beta != 0.0f) out = fmaf(beta, load_c(p, off), out);
-      store_c(p, off, out);
+  const bool active = lane < CW && j < p.Nv;
+  const int rows = min(32, p.Mv - row0);
+  int64_t off = cbase + static_cast<int64_t>(row0) * p.ldc + j;
+#pragma unroll
+  for (int g = 0; g < 32; g += G) {
+    float w[G];
+#pragma unroll
+    for (int r = 0; r < G; ++r) w[r] = stg[(g + r) * kEpiPitch + lane];
+    if (active) {
+      if (beta != 0.0f) {
+        float cin[G];
+        int64_t o = off;
+#pragma unroll
+        for (int r = 0; r < G; ++r, o += p.ldc)
+          if (g + r < rows) cin[r] = load_c(p, o);
+#pragma unroll
+        for (int r = 0; r < G; ++r) w[r] = fmaf(beta, cin[r], w[r]);
+      }
+#pragma unroll
+      for (int r = 0; r < G; ++r, off += p.ldc)
+        if (g + r < rows) store_c(p, off, w[r]);
     }
   }
+  __syncwarp();  // staging tile free for the next chunk
+}
+
+// One chunk of 32 accumulator columns -> C through a TMA box store.  The
+// warp writes its 32 rows into a 4 KB box buffer laid out with the tensor
+// map's swizzle (128-byte rows for fp32, 64-byte rows for bf16), then one
+// lane stores the box; TMA clips rows and columns outside C.  Two buffers
+// per warp alternate, so a box is written while the previous one drains.
+__device__ __forceinline__ void store_chunk_tma(const KParams& p, const CUtensorMap* tmC,
+                                                float (&v)[32], uint8_t* box, uint32_t box_addr,
+                                                int lane, int row0, int col0, int b) {
+  const float alpha = p.alpha;
+  if (lane == 0) bulk_wait_group_read<1>();  // this buffer's previous box has been read
   __syncwarp();
+  if (!p.c_bf16) {
+    uint8_t* row = box + lane * 128;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      *reinterpret_cast<float4*>(row + ((j ^ (lane & 7)) << 4)) =
+          make_float4(alpha * v[4 * j], alpha * v[4 * j + 1], alpha * v[4 * j + 2],
+                      alpha * v[4 * j + 3]);
+  } else {
+    uint8_t* row = box + lane * 64;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint32_t w[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const __nv_bfloat162 h =
+            __floats2bfloat162_rn(alpha * v[8 * j + 2 * e], alpha * v[8 * j + 2 * e + 1]);
+        w[e] = *reinterpret_cast<const uint32_t*>(&h);
+      }
+      *reinterpret_cast<uint4*>(row + ((j ^ ((lane >> 1) & 3)) << 4)) =
+          make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+  fence_proxy_async_shared();
+  __syncwarp();
+  if (lane == 0 && row0 < p.Mv && col0 < p.Nv) {  // boxes wholly outside C are skipped
+    tma_store_3d(tmC, box_addr, col0, row0, b);
+    bulk_commit_group();
+  }
 }
 
 template <int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     bmm_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUtensorMap tmA,
-                  const __grid_constant__ CUtensorMap tmB) {
+                  const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmC) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
@@ -232,6 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if (p.c_tma) tma_prefetch_desc(&tmC);
   }
   if (warp == 1) {
     tmem_alloc(smem_addr(tmem_slot), p.tmem_cols);
@@ -255,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int za = p.a_bcast ? 0 : b, zb = p.b_bcast ? 0 : b;
         for (int kb = 0; kb < p.k_blocks; ++kb, ++it) {
           const uint32_t s = it % S, ph = (it / S) & 1u;
-          if (!wait_bounded(empty_bar(s), ph ^ 1u, ab, kSiteProducerEmpty)) {
+          if (!wait_bounded<true>(empty_bar(s), ph ^ 1u, ab, kSiteProducerEmpty)) {
             ok = false;
             break;
           }
@@ -289,10 +376,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t a_lbo = p.a_mn ? 8192u : 16u, b_lbo = p.b_mn ? 8192u : 16u;
       const uint32_t a_step = p.a_mn ? 2048u : 32u, b_step = p.b_mn ? 2048u : 32u;
       uint32_t it = 0, tl = 0;
-      bool ok = true;
+      // Failure-detection test: phase 0 of the drain barrier completes only
+      // after this thread's final commit, so this wait must run out.
+      bool ok = !p.test_stall || wait_bounded(drain_bar, 0u, ab, kSiteTestStall);
       for (int64_t t = blockIdx.x; t < p.tiles && ok; t += gridDim.x, ++tl) {
         const uint32_t acc = tl & 1u, aph = (tl >> 1) & 1u;
-        if (!wait_bounded(acce_bar(acc), aph ^ 1u, ab, kSiteMmaAccEmpty)) {
+        if (!wait_bounded<true>(acce_bar(acc), aph ^ 1u, ab, kSiteMmaAccEmpty)) {
           ok = false;
           break;
         }
@@ -300,11 +389,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t d_tmem = tmem_base + acc * BN;
         for (int kb = 0; kb < p.k_blocks; ++kb, ++it) {
           const uint32_t s = it % S, ph = (it / S) & 1u;
-          if (!wait_bounded(full_bar(s), ph, ab, kSiteMmaFull)) {
+          if (!wait_bounded<true>(full_bar(s), ph, ab, kSiteMmaFull)) {
             ok = false;
             break;
           }
-          tc_fence_after_sync();
+          // No tcgen05 fence here: the TMA writes and the MMA reads of this
+          // slot are both async-proxy operations ordered by the barrier's
+          // transaction count, and a fence inside the accumulation chain
+          // stalls the tensor pipe (about a third of its throughput).
           const uint32_t a_addr = sbase + s * p.stage_bytes;
           const uint32_t b_addr = a_addr + p.a_bytes;
           const int nsteps = (kb == p.k_blocks - 1) ? p.tail_steps : kTileK / kUmmaK;
@@ -327,6 +419,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // --------------------------------------------------------- epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     float* stg = epi + (warp - 2) * 32 * kEpiPitch;
+    uint8_t* boxes = reinterpret_cast<uint8_t*>(epi) + (warp - 2) * 2 * kEpiBoxBytes;
+    const uint32_t boxes_addr = smem_addr(boxes);
+    uint32_t nbox = 0;
     uint32_t tl = 0;
     for (int64_t t = blockIdx.x; t < p.tiles; t += gridDim.x, ++tl) {
       const uint32_t acc = tl & 1u, aph = (tl >> 1) & 1u;
@@ -360,10 +455,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(acce_bar(acc));  // accumulator may be reused
           }
-          store_chunk<32>(p, v, stg, lane, row0, nb * BN + 32 * c, cbase);
+          if (p.c_tma) {
+            const uint32_t k = nbox++ & 1u;
+            store_chunk_tma(p, &tmC, v, boxes + k * kEpiBoxBytes, boxes_addr + k * kEpiBoxBytes,
+                            lane, row0, nb * BN + 32 * c, b);
+          } else {
+            store_chunk<32>(p, v, stg, lane, row0, nb * BN + 32 * c, cbase);
+          }
         }
       }
     }
+    if (lane == 0) bulk_wait_group_all();  // box stores done before shared memory is released
   }
 
   __syncwarp();
@@ -373,19 +475,244 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem_base, p.tmem_cols);
 }
 
+// bmm_tc2_kernel: the same pipeline over CTA pairs (a cluster of 2).  The
+// pair computes a 256 x BN tile with tcgen05.mma.cta_group::2: CTA r holds
+// rows [128r, 128r+128) of the A tile and rows [r*BN/2, (r+1)*BN/2) of the
+// K x BN B tile in its own ring stage (32 KB at BN = 256), so each SM takes in
+// a third less operand data per FLOP than a 1-CTA 128 x 256 tile and its
+// tensor core reads half of B from the peer's shared memory.
+//   - Both CTAs' TMA loads count on the leader's "full" barrier (the leader
+//     expects the bytes of both halves); only the leader waits on it.
+//   - The leader's single MMA thread issues 256 x BN x 16 MMAs and
+//     multicasts each tcgen05.commit to the "empty" (slot) and "acc full"
+//     barriers of both CTAs.
+//   - Each CTA's epilogue drains its own 128 accumulator rows; the peer's
+//     four warps release the accumulator by arriving on the leader's "acc
+//     empty" barrier (8 arrivals per phase).
+//   - A cluster barrier at the end keeps either CTA from exiting (or freeing
+//     Tensor Memory) while the other can still signal it.
+template <int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+    bmm_tc2_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUtensorMap tmA,
+                   const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmC) {
+  constexpr int BNH = BN / 2;  // B tile rows held by each CTA
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
+  uint8_t* smem = smem_raw + pad;
+  const uint32_t sbase = raw + pad;
+
+  const int S = p.stages;
+  const uint32_t ring_bytes = static_cast<uint32_t>(S) * p.stage_bytes;
+  float* epi = reinterpret_cast<float*>(smem + ring_bytes);
+  const uint32_t bar0 = sbase + ring_bytes + kEpiBytes;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + ring_bytes + kEpiBytes + 8u * (2u * S + 5u));
+  volatile uint32_t* abort_flag = tmem_slot + 1;
+
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
+  auto accf_bar = [&](int a) { return bar0 + 8u * (2 * S + a); };
+  auto acce_bar = [&](int a) { return bar0 + 8u * (2 * S + 2 + a); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * S + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int64_t pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(accf_bar(a), 1);
+      mbar_init(acce_bar(a), 8);  // four epilogue warps in each CTA of the pair
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0u;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    if (p.c_tma) tma_prefetch_desc(&tmC);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_addr(tmem_slot), p.tmem_cols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  cluster_sync();  // both CTAs' barriers are initialised before any cross-CTA signal
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+  const Abort ab{abort_flag, p.err, p.timeout_ns};
+
+  if (warp == 0) {
+    // --------------------------------------------- TMA producer (each CTA)
+    if (lane == 0) {
+      uint32_t it = 0;
+      bool ok = true;
+      for (int64_t t = pair; t < p.tiles && ok; t += npairs) {
+        int b, mb, nb;
+        decode_tile(t, p, b, mb, nb);
+        const int m_own = mb * (2 * kTileM) + static_cast<int>(rank) * kTileM;
+        const int n_own = nb * BN + static_cast<int>(rank) * BNH;
+        const int za = p.a_bcast ? 0 : b, zb = p.b_bcast ? 0 : b;
+        for (int kb = 0; kb < p.k_blocks; ++kb, ++it) {
+          const uint32_t s = it % S, ph = (it / S) & 1u;
+          if (!wait_bounded<true>(empty_bar(s), ph ^ 1u, ab, kSiteProducerEmpty)) {
+            ok = false;
+            break;
+          }
+          const uint32_t a_dst = sbase + s * p.stage_bytes;
+          const uint32_t b_dst = a_dst + p.a_bytes;
+          if (leader) mbar_arrive_expect_tx(full_bar(s), 2u * p.tx_bytes);
+          const uint32_t fb = mapa_shared(full_bar(s), 0);  // the leader's barrier
+          const int k0 = kb * kTileK;
+          if (!p.a_mn) {
+            tma_load_3d_pair(a_dst, &tmA, fb, k0, m_own, za);
+          } else {
+            tma_load_3d_pair(a_dst, &tmA, fb, m_own, k0, za);
+            tma_load_3d_pair(a_dst + 8192u, &tmA, fb, m_own + 64, k0, za);
+          }
+          if (!p.b_mn) {
+            tma_load_3d_pair(b_dst, &tmB, fb, k0, n_own, zb);
+          } else {
+#pragma unroll
+            for (int h = 0; h < BNH / 64; ++h)
+              tma_load_3d_pair(b_dst + 8192u * h, &tmB, fb, n_own + 64 * h, k0, zb);
+          }
+        }
+      }
+      // The leader's full barriers count both CTAs' bytes: once the last S
+      // have completed, no load of either CTA is still in flight.
+      if (leader) {
+        const uint32_t first = it > static_cast<uint32_t>(S) ? it - S : 0u;
+        for (uint32_t j = first; j < it; ++j) drain_wait(full_bar(j % S), (j / S) & 1u);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------- MMA issuer (leader only)
+    if (lane == 0 && leader) {
+      const uint32_t a_lbo = p.a_mn ? 8192u : 16u, b_lbo = p.b_mn ? 8192u : 16u;
+      const uint32_t a_step = p.a_mn ? 2048u : 32u, b_step = p.b_mn ? 2048u : 32u;
+      uint32_t it = 0, tl = 0;
+      bool ok = !p.test_stall || wait_bounded(drain_bar, 0u, ab, kSiteTestStall);
+      for (int64_t t = pair; t < p.tiles && ok; t += npairs, ++tl) {
+        const uint32_t acc = tl & 1u, aph = (tl >> 1) & 1u;
+        if (!wait_bounded<true>(acce_bar(acc), aph ^ 1u, ab, kSiteMmaAccEmpty)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = 0; kb < p.k_blocks; ++kb, ++it) {
+          const uint32_t s = it % S, ph = (it / S) & 1u;
+          if (!wait_bounded<true>(full_bar(s), ph, ab, kSiteMmaFull)) {
+            ok = false;
+            break;
+          }
+          // No tcgen05 fence here: the TMA writes and the MMA reads of this
+          // slot are both async-proxy operations ordered by the barrier's
+          // transaction count, and a fence inside the accumulation chain
+          // stalls the tensor pipe (about a third of its throughput).
+          const uint32_t a_addr = sbase + s * p.stage_bytes;
+          const uint32_t b_addr = a_addr + p.a_bytes;
+          const int nsteps = (kb == p.k_blocks - 1) ? p.tail_steps : kTileK / kUmmaK;
+          for (int ks = 0; ks < nsteps; ++ks) {
+            const uint64_t ad = smem_desc_sw128(a_addr + ks * a_step, a_lbo, 1024u);
+            const uint64_t bd = smem_desc_sw128(b_addr + ks * b_step, b_lbo, 1024u);
+            tc_mma_f16_pair(d_tmem, ad, bd, p.idesc, (kb > 0 || ks > 0) ? 1u : 0u);
+          }
+          tc_commit_pair_multicast(empty_bar(s), 0x3);  // slot free in both CTAs
+        }
+        if (!ok) break;
+        tc_commit_pair_multicast(accf_bar(acc), 0x3);  // accumulator halves complete
+      }
+      tc_commit_pair(drain_bar);
+      drain_wait(drain_bar, 0u);
+    }
+  } else {
+    // ------------------------------------------------ epilogue (each CTA)
+    const int q = warp & 3;
+    float* stg = epi + (warp - 2) * 32 * kEpiPitch;
+    uint8_t* boxes = reinterpret_cast<uint8_t*>(epi) + (warp - 2) * 2 * kEpiBoxBytes;
+    const uint32_t boxes_addr = smem_addr(boxes);
+    uint32_t nbox = 0;
+    const uint32_t acce_leader0 = mapa_shared(acce_bar(0), 0);
+    const uint32_t acce_leader1 = mapa_shared(acce_bar(1), 0);
+    uint32_t tl = 0;
+    for (int64_t t = pair; t < p.tiles; t += npairs, ++tl) {
+      const uint32_t acc = tl & 1u, aph = (tl >> 1) & 1u;
+      int ok = 1;
+      if (lane == 0) ok = wait_bounded(accf_bar(acc), aph, ab, kSiteEpiAccFull) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      __syncwarp();
+      tc_fence_after_sync();
+      int b, mb, nb;
+      decode_tile(t, p, b, mb, nb);
+      const int row0 = mb * (2 * kTileM) + static_cast<int>(rank) * kTileM + q * 32;
+      const int64_t cbase = static_cast<int64_t>(b) * p.sC;
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        float v[32];
+        tmem_ld_32cols(taddr + 32u * c, v);
+        tmem_wait_ld();
+        if (c == BN / 32 - 1) {
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(acc ? acce_leader1 : acce_leader0);
+        }
+        if (p.c_tma) {
+          const uint32_t k = nbox++ & 1u;
+          store_chunk_tma(p, &tmC, v, boxes + k * kEpiBoxBytes, boxes_addr + k * kEpiBoxBytes,
+                          lane, row0, nb * BN + 32 * c, b);
+        } else {
+          store_chunk<32>(p, v, stg, lane, row0, nb * BN + 32 * c, cbase);
+        }
+      }
+    }
+    if (lane == 0) bulk_wait_group_all();
+  }
+
+  __syncwarp();
+  tc_fence_before_sync();
+  __syncthreads();
+  cluster_sync();  // no CTA of the pair signals the other after this point
+  tc_fence_after_sync();
+  if (warp == 1) tmem_dealloc_pair(tmem_base, p.tmem_cols);
+}
+
 // Copy a strided 16-bit operand into the workspace with ld rounded up to a
 // multiple of 8 elements (16 bytes), which TMA needs for its row strides.
+// Each thread moves one 8-element segment of a row: eight 2-byte loads (the
+// source rows need not be aligned) and one 16-byte store (destination rows
+// are).  Columns past the row end are written as zero; TMA never reads them.
 __global__ void pack16_kernel(const uint16_t* __restrict__ src, uint16_t* __restrict__ dst,
                               int64_t nb, int64_t rows, int64_t cols, int64_t ld_src,
                               int64_t s_src, int64_t ld_dst, int64_t s_dst) {
-  const int64_t total_rows = nb * rows;
-  for (int64_t r = blockIdx.y; r < total_rows; r += gridDim.y) {
-    const int64_t b = r / rows, i = r - b * rows;
-    const uint16_t* s = src + b * s_src + i * ld_src;
-    uint16_t* d = dst + b * s_dst + i * ld_dst;
-    for (int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; c < cols;
-         c += static_cast<int64_t>(gridDim.x) * blockDim.x)
-      d[c] = s[c];
+  const int64_t segs = (cols + 7) / 8;
+  const int64_t total = nb * rows * segs;
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < total;
+       t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t row = t / segs, seg = t - row * segs;
+    const int64_t b = row / rows, i = row - b * rows;
+    const uint16_t* s = src + b * s_src + i * ld_src + seg * 8;
+    const int64_t n = (cols - seg * 8) < 8 ? (cols - seg * 8) : 8;
+    uint16_t e[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) e[k] = k < n ? s[k] : static_cast<uint16_t>(0);
+    uint4 q;
+    q.x = e[0] | (static_cast<uint32_t>(e[1]) << 16);
+    q.y = e[2] | (static_cast<uint32_t>(e[3]) << 16);
+    q.z = e[4] | (static_cast<uint32_t>(e[5]) << 16);
+    q.w = e[6] | (static_cast<uint32_t>(e[7]) << 16);
+    *reinterpret_cast<uint4*>(dst + b * s_dst + i * ld_dst + seg * 8) = q;
   }
 }
 

@@ -97,9 +97,10 @@ typedef struct {
   int32_t pack_a, pack_b;         /* 1: operand staged through the workspace */
   int32_t even_k;                 /* 1: K is a multiple of tile_k (no tail tile) */
   int32_t tmem_cols;              /* Tensor Memory columns allocated per CTA */
+  int32_t cta_pair;               /* 1: tiles run on CTA pairs (2-SM MMA, tile_m = 256) */
   int64_t tiles;                  /* output tiles over the whole batch */
   int64_t smem_bytes;             /* dynamic shared memory per CTA */
-  int64_t stage_bytes;            /* bytes of one ring stage (A tile + B tile) */
+  int64_t stage_bytes;            /* bytes of one CTA's ring stage (its A and B tile parts) */
   int64_t workspace_bytes;        /* device workspace the plan owns */
 } bmm_plan_info_t;
 

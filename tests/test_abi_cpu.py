@@ -109,9 +109,10 @@ def _stage_bytes_formula(bm, bn, bk, esz=2):
 def test_planner_on_workloads(lib, name):
     p = wl.WORKLOADS[name]
     info = api.bmm_plan_query(desc_for(p))
-    assert info.tile_m == 128 and info.tile_k == 64
+    assert info.tile_m == (256 if info.cta_pair else 128) and info.tile_k == 64
     assert info.smem_bytes <= SMEM_LIMIT
-    raw = _stage_bytes_formula(info.tile_m, info.tile_n, info.tile_k)
+    # one CTA's share of the tile: all of a 128-row A tile, half of B on a pair
+    raw = _stage_bytes_formula(128, info.tile_n // (2 if info.cta_pair else 1), info.tile_k)
     assert info.stage_bytes == -(-raw // 1024) * 1024
     assert info.stages * info.stage_bytes <= SMEM_LIMIT
     assert info.stages >= 4
@@ -121,8 +122,15 @@ def test_planner_on_workloads(lib, name):
         assert info.swap_ab == 1 and info.tile_n == 16
         assert info.tiles == p.batch * 2          # N=256 over two 128-row MMA tiles
     if p is wl.GEMM_4096:
-        assert info.tile_n == 256 and info.tiles == 32 * 16 and info.stages == 4
+        # CTA pairs with 256 x 224 tiles: 16 x 19 = 304 tiles = exactly 4 rounds
+        # on 76 pairs (256-wide tiles would leave a 0.37 wave); 30 KB per CTA
+        # per stage, six stages
+        assert info.cta_pair == 1 and info.tile_n == 224 and info.tiles == 16 * 19
+        assert info.stages == 6 and info.tmem_cols == 512
         assert info.workspace_bytes == 0
+    if p is wl.ATTN_QK:
+        # 8192 pair tiles of 256 x 256 fill 108 rounds almost exactly
+        assert info.cta_pair == 1 and info.tile_n == 256 and info.tiles == 128 * 8 * 8
     if p is wl.RAGGED:
         # B stored K x N with ld 999 (not a multiple of 8): staged; A (ld 1000) read in place
         assert info.pack_b == 1 and info.pack_a == 0
@@ -138,3 +146,24 @@ def test_planner_boundary_shapes(lib):
                                         strideA=M * 48, strideB=48 * 96, strideC=M * 96))
         assert info.even_k == 0
         assert info.tiles >= 1
+
+
+def test_pair_mode_can_be_switched_off(lib, monkeypatch):
+    monkeypatch.setenv("DMT_BMM_PAIR", "0")
+    info = api.bmm_plan_query(desc_for(wl.GEMM_4096))
+    # single CTAs: 128 x 224 tiles, 32 x 19 = 608 = 4 rounds on 152 SMs
+    assert info.cta_pair == 0 and info.tile_m == 128 and info.tile_n == 224
+    assert info.tiles == 32 * 19 and info.stages == 4
+    monkeypatch.setenv("DMT_BMM_PAIR", "1")
+    assert api.bmm_plan_query(desc_for(wl.GEMM_4096)).cta_pair == 1
+
+
+def test_wave_balanced_tile_width(lib, monkeypatch):
+    # the estimate rounds x tile_n picks the width with the least idle tail
+    info = api.bmm_plan_query(desc_for(wl.RAGGED))
+    assert info.cta_pair == 1 and info.tile_n == 256      # 256 tiles -> 4 rounds of 256
+    monkeypatch.setenv("DMT_BMM_TILE_N", "192")
+    assert api.bmm_plan_query(desc_for(wl.GEMM_4096)).tile_n == 192
+    monkeypatch.setenv("DMT_BMM_TILE_N", "224")
+    # MN-major B on a pair is loaded in 64-column boxes per CTA: 224 is not allowed
+    assert api.bmm_plan_query(desc_for(wl.RAGGED)).tile_n == 256

@@ -104,6 +104,23 @@ def test_padded_and_unaligned_leading_dimensions():
     check_full(p, x, c)
 
 
+@pytest.mark.parametrize("N,tc", [(260, "bf16"), (264, "bf16"), (258, "f32"), (260, "f32")])
+def test_box_store_edges(N, tc):
+    """Row-major C with padded ldc: rows whose byte length is a multiple of
+    16 go out through TMA box stores, the others through direct stores; the
+    padding between rows and the guard after C must stay untouched."""
+    p = wl.Problem(batch=2, M=130, N=N, K=72, transB=True, type_ab="bf16", type_c=tc,
+                   ldc=N + 12, seed=83 + N)
+    x = wl.make_inputs(p)
+    c, _ = run_gpu(p, x, c_fill="garbage")
+    check_full(p, x, c)
+    s = p.strides()
+    pad = np.concatenate([np.arange(b * s["sC"] + i * s["ldc"] + p.N, b * s["sC"] + (i + 1) * s["ldc"])
+                          for b in range(p.batch) for i in range(p.M - 1)])
+    fill = np.float32(7.0) if tc == "f32" else np.uint16(0x40E0)
+    assert np.all(c[pad] == fill)
+
+
 def test_padded_aligned_leading_dimensions():
     p = wl.Problem(batch=2, M=130, N=260, K=100, transB=True, type_ab="bf16", type_c="bf16",
                    lda=136, ldb=112, ldc=272, sA=136 * 130 + 8, seed=82)
@@ -170,13 +187,56 @@ def test_repeated_runs_and_streams():
     check_full(p, x, first)
 
 
+# ------------------------------------------------- 1-CTA and CTA-pair tiles
+
+@pytest.mark.parametrize("pair", ["1", "0"])
+@pytest.mark.parametrize("transA,transB", list(itertools.product([False, True], repeat=2)))
+def test_large_tile_class_both_kernels(pair, transA, transB, monkeypatch):
+    """The 256-wide tile class runs on CTA pairs (2-SM MMA) by default and on
+    single CTAs with DMT_BMM_PAIR=0; both must meet the tolerance, with
+    ragged M, N and K tails and several tiles per CTA."""
+    monkeypatch.setenv("DMT_BMM_PAIR", pair)
+    p = wl.Problem(batch=2, M=1100, N=600, K=333, transA=transA, transB=transB, type_ab="bf16",
+                   type_c="f32", alpha=1.5, beta=-0.5, dist_ab="normal", seed=91)
+    x = wl.make_inputs(p)
+    c, info = run_gpu(p, x)
+    assert info.cta_pair == int(pair) and info.tile_n >= 192
+    check_full(p, x, c)
+
+
+@pytest.mark.parametrize("type_c", ["f32", "bf16"])
+def test_tile_configuration_does_not_change_exact_results(monkeypatch, type_c):
+    """Changing the tile configuration must never change the output
+    ("Optimize Triton Block Parameters", Correctness requirements).  With
+    small integers every fp32 sum is exact, so every tile width on both
+    kernels must match the oracle and each other bit for bit (for bf16 output
+    the single rounding of those exact sums must agree too).  M, N, K are
+    ragged against every tile."""
+    p = wl.Problem(batch=2, M=520, N=1000, K=1000, transB=True, type_ab="bf16", type_c=type_c,
+                   seed=92)
+    na, nb, _ = p.storage_elems()
+    x = wl.Inputs(wl.small_ints16(na, 921, -2, 2, "bf16"), wl.small_ints16(nb, 922, -2, 2, "bf16"), None)
+    out = {}
+    for pair in ("1", "0"):
+        for tn in ("192", "224", "256"):
+            monkeypatch.setenv("DMT_BMM_PAIR", pair)
+            monkeypatch.setenv("DMT_BMM_TILE_N", tn)
+            out[pair, tn], info = run_gpu(p, x)
+            assert info.cta_pair == int(pair) and info.tile_n == int(tn)
+            if type_c == "f32":
+                check_full(p, x, out[pair, tn], exact=True)
+    first = out["1", "256"]
+    for k, v in out.items():
+        assert np.array_equal(v, first), k
+
+
 # ------------------------------------------------------- full-size workloads
 
 def test_workload_gemm_4096():
     p = wl.GEMM_4096
     x = wl.make_inputs(p)
     c, info = run_gpu(p, x, guard=8192)
-    assert info.tile_n == 256 and info.even_k == 1 and info.swap_ab == 0
+    assert info.tile_n == 224 and info.cta_pair == 1 and info.even_k == 1 and info.swap_ab == 0
     check_sampled(p, x, c, sample_indices(p, 3000, 1))
 
 
