@@ -139,6 +139,45 @@ __device__ __noinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   }
 }
 
+// Shared-memory descriptor words: the low word carries the start address
+// (>> 4) and the leading byte offset, the high word the stride byte offset,
+// the version and the 128-byte swizzle.  Start addresses stay below 256 KB,
+// so stepping the low word by (bytes >> 4) never carries into the LBO field.
+__device__ __forceinline__ uint32_t desc_lo(uint32_t saddr, uint32_t lbo) {
+  return ((saddr >> 4) & 0x3FFFu) | (((lbo >> 4) & 0x3FFFu) << 16);
+}
+__device__ __forceinline__ uint32_t desc_hi_sw128(uint32_t sbo) {
+  return ((sbo >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
+}
+__device__ __forceinline__ uint64_t desc_join(uint32_t lo, uint32_t hi) {
+  return (static_cast<uint64_t>(hi) << 32) | lo;
+}
+
+// MMAs of one k-block (4 k-steps of 16, or `nsteps` on a ragged tail) with
+// the descriptors stepped by (k-step bytes >> 4) in their low words.
+template <bool kPair>
+__device__ __forceinline__ void issue_kblock(uint32_t d_tmem, uint32_t alo, uint32_t blo,
+                                             uint32_t ahi, uint32_t bhi, uint32_t astep,
+                                             uint32_t bstep, uint32_t idesc, int nsteps,
+                                             bool first) {
+  if (nsteps == kTileK / kUmmaK) {
+#pragma unroll
+    for (int ks = 0; ks < kTileK / kUmmaK; ++ks) {
+      const uint64_t ad = desc_join(alo + ks * astep, ahi), bd = desc_join(blo + ks * bstep, bhi);
+      const uint32_t acc = (!first || ks > 0) ? 1u : 0u;
+      if (kPair) tc_mma_f16_pair(d_tmem, ad, bd, idesc, acc);
+      else tc_mma_f16(d_tmem, ad, bd, idesc, acc);
+    }
+  } else {
+    for (int ks = 0; ks < nsteps; ++ks) {
+      const uint64_t ad = desc_join(alo + ks * astep, ahi), bd = desc_join(blo + ks * bstep, bhi);
+      const uint32_t acc = (!first || ks > 0) ? 1u : 0u;
+      if (kPair) tc_mma_f16_pair(d_tmem, ad, bd, idesc, acc);
+      else tc_mma_f16(d_tmem, ad, bd, idesc, acc);
+    }
+  }
+}
+
 __device__ __forceinline__ void decode_tile(int64_t t, const KParams& p, int& b, int& mb, int& nb) {
   const int64_t per = static_cast<int64_t>(p.num_m) * p.num_n;
   b = static_cast<int>(t / per);
@@ -373,9 +412,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      const uint32_t a_lbo = p.a_mn ? 8192u : 16u, b_lbo = p.b_mn ? 8192u : 16u;
-      const uint32_t a_step = p.a_mn ? 2048u : 32u, b_step = p.b_mn ? 2048u : 32u;
-      uint32_t it = 0, tl = 0;
+      // Descriptor words for stage 0; stage s adds s * (stage_bytes >> 4).
+      const uint32_t alo0 = desc_lo(sbase, p.a_mn ? 8192u : 16u);
+      const uint32_t blo0 = desc_lo(sbase + p.a_bytes, p.b_mn ? 8192u : 16u);
+      const uint32_t hi = desc_hi_sw128(1024u);
+      const uint32_t astep = (p.a_mn ? 2048u : 32u) >> 4, bstep = (p.b_mn ? 2048u : 32u) >> 4;
+      const uint32_t sstep = p.stage_bytes >> 4;
+      uint32_t s = 0, ph = 0, tl = 0;
       // Failure-detection test: phase 0 of the drain barrier completes only
       // after this thread's final commit, so this wait must run out.
       bool ok = !p.test_stall || wait_bounded(drain_bar, 0u, ab, kSiteTestStall);
@@ -387,8 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + acc * BN;
-        for (int kb = 0; kb < p.k_blocks; ++kb, ++it) {
-          const uint32_t s = it % S, ph = (it / S) & 1u;
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
           if (!wait_bounded<true>(full_bar(s), ph, ab, kSiteMmaFull)) {
             ok = false;
             break;
@@ -396,16 +438,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           // No tcgen05 fence here: the TMA writes and the MMA reads of this
           // slot are both async-proxy operations ordered by the barrier's
           // transaction count, and a fence inside the accumulation chain
-          // stalls the tensor pipe (about a third of its throughput).
-          const uint32_t a_addr = sbase + s * p.stage_bytes;
-          const uint32_t b_addr = a_addr + p.a_bytes;
+          // stalls the tensor pipe.
           const int nsteps = (kb == p.k_blocks - 1) ? p.tail_steps : kTileK / kUmmaK;
-          for (int ks = 0; ks < nsteps; ++ks) {
-            const uint64_t ad = smem_desc_sw128(a_addr + ks * a_step, a_lbo, 1024u);
-            const uint64_t bd = smem_desc_sw128(b_addr + ks * b_step, b_lbo, 1024u);
-            tc_mma_f16(d_tmem, ad, bd, p.idesc, (kb > 0 || ks > 0) ? 1u : 0u);
-          }
+          issue_kblock<false>(d_tmem, alo0 + s * sstep, blo0 + s * sstep, hi, hi, astep, bstep,
+                              p.idesc, nsteps, kb == 0);
           tc_commit(empty_bar(s));  // slot is free once these MMAs have read it
+          if (++s == static_cast<uint32_t>(S)) {
+            s = 0;
+            ph ^= 1u;
+          }
         }
         if (!ok) break;
         tc_commit(accf_bar(acc));  // accumulator complete
@@ -597,9 +638,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------- MMA issuer (leader only)
     if (lane == 0 && leader) {
-      const uint32_t a_lbo = p.a_mn ? 8192u : 16u, b_lbo = p.b_mn ? 8192u : 16u;
-      const uint32_t a_step = p.a_mn ? 2048u : 32u, b_step = p.b_mn ? 2048u : 32u;
-      uint32_t it = 0, tl = 0;
+      const uint32_t alo0 = desc_lo(sbase, p.a_mn ? 8192u : 16u);
+      const uint32_t blo0 = desc_lo(sbase + p.a_bytes, p.b_mn ? 8192u : 16u);
+      const uint32_t hi = desc_hi_sw128(1024u);
+      const uint32_t astep = (p.a_mn ? 2048u : 32u) >> 4, bstep = (p.b_mn ? 2048u : 32u) >> 4;
+      const uint32_t sstep = p.stage_bytes >> 4;
+      uint32_t s = 0, ph = 0, tl = 0;
       bool ok = !p.test_stall || wait_bounded(drain_bar, 0u, ab, kSiteTestStall);
       for (int64_t t = pair; t < p.tiles && ok; t += npairs, ++tl) {
         const uint32_t acc = tl & 1u, aph = (tl >> 1) & 1u;
@@ -609,25 +653,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + acc * BN;
-        for (int kb = 0; kb < p.k_blocks; ++kb, ++it) {
-          const uint32_t s = it % S, ph = (it / S) & 1u;
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
           if (!wait_bounded<true>(full_bar(s), ph, ab, kSiteMmaFull)) {
             ok = false;
             break;
           }
-          // No tcgen05 fence here: the TMA writes and the MMA reads of this
-          // slot are both async-proxy operations ordered by the barrier's
-          // transaction count, and a fence inside the accumulation chain
-          // stalls the tensor pipe (about a third of its throughput).
-          const uint32_t a_addr = sbase + s * p.stage_bytes;
-          const uint32_t b_addr = a_addr + p.a_bytes;
+          // No tcgen05 fence here (see the single-CTA kernel).
           const int nsteps = (kb == p.k_blocks - 1) ? p.tail_steps : kTileK / kUmmaK;
-          for (int ks = 0; ks < nsteps; ++ks) {
-            const uint64_t ad = smem_desc_sw128(a_addr + ks * a_step, a_lbo, 1024u);
-            const uint64_t bd = smem_desc_sw128(b_addr + ks * b_step, b_lbo, 1024u);
-            tc_mma_f16_pair(d_tmem, ad, bd, p.idesc, (kb > 0 || ks > 0) ? 1u : 0u);
-          }
+          issue_kblock<true>(d_tmem, alo0 + s * sstep, blo0 + s * sstep, hi, hi, astep, bstep,
+                             p.idesc, nsteps, kb == 0);
           tc_commit_pair_multicast(empty_bar(s), 0x3);  // slot free in both CTAs
+          if (++s == static_cast<uint32_t>(S)) {
+            s = 0;
+            ph ^= 1u;
+          }
         }
         if (!ok) break;
         tc_commit_pair_multicast(accf_bar(acc), 0x3);  // accumulator halves complete
