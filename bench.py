@@ -50,9 +50,13 @@ MEASURED_FALLBACK = {"hbm_gbs": 6676.5, "bf16_tflops": 1932.9, "bf16_tflops_sust
                      "sm_max_mhz": 2070.0}
 RECIPE_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
-# DRAM traffic per launch of the dominant kernel from one ncu capture, keyed by
-# a hash of the kernel sources: reported only while the sources are unchanged.
-NCU_TRAFFIC = {}
+# DRAM traffic per launch of the dominant kernel from one ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum; profiles/ has the summary),
+# keyed by a hash of the kernel sources and the workload: reported only while
+# the sources are unchanged.
+NCU_TRAFFIC = {
+    ("d8808b2f9b9223ff", "gemm_4096x4096x4096_tn_bf16"): 85147392 + 17099520,
+}
 
 FLUSH_BYTES = 512 << 20
 
@@ -88,6 +92,8 @@ def parse():
     ap.add_argument("--no-other", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the cpu_baseline leg")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the workload's batch count (small cases for profiling)")
     return ap.parse_args()
 
 
@@ -359,8 +365,11 @@ def dist_env():
 def main():
     args = parse()
     world, rank, local = dist_env()
+    import dataclasses
     from dense_matmul_tensor_gb300 import workloads as wl
     p = wl.WORKLOADS[args.workload]
+    if args.batch is not None:
+        p = dataclasses.replace(p, batch=args.batch, name=f"{p.name}@batch{args.batch}")
 
     if args.impl == "reference":
         if rank != 0:
@@ -427,7 +436,7 @@ def main():
     achieved = p.flops() / (ms_mean * 1e-3) / 1e12
     roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
             "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
-            "traffic": NCU_TRAFFIC.get(kernel_source_hash()),
+            "traffic": NCU_TRAFFIC.get((kernel_source_hash(), p.name)),
             "kernel": (f"bmm_tc2_kernel<{info.tile_n}> (CTA pairs)" if info.cta_pair
                        else f"bmm_tc_kernel<{info.tile_n}>"),
             "peak_source": f"{peak_src} bf16 burst",
