@@ -249,21 +249,32 @@ __device__ __forceinline__ void store_chunk(const KParams& p, float (&v)[CW], fl
   const bool active = lane < CW && j < p.Nv;
   const int rows = min(32, p.Mv - row0);
   int64_t off = cbase + static_cast<int64_t>(row0) * p.ldc + j;
+  if (beta != 0.0f) {
+    // All 32 rows of C_in are requested before anything is stored: one
+    // memory latency per chunk instead of one per group of rows.
+    float cin[32];
+    int64_t o = off;
+#pragma unroll
+    for (int r = 0; r < 32; ++r, o += p.ldc)
+      if (active && r < rows) cin[r] = load_c(p, o);
+#pragma unroll
+    for (int g = 0; g < 32; g += G) {
+      float w[G];
+#pragma unroll
+      for (int r = 0; r < G; ++r) w[r] = fmaf(beta, cin[g + r], stg[(g + r) * kEpiPitch + lane]);
+#pragma unroll
+      for (int r = 0; r < G; ++r, off += p.ldc)
+        if (active && g + r < rows) store_c(p, off, w[r]);
+    }
+    __syncwarp();
+    return;
+  }
 #pragma unroll
   for (int g = 0; g < 32; g += G) {
     float w[G];
 #pragma unroll
     for (int r = 0; r < G; ++r) w[r] = stg[(g + r) * kEpiPitch + lane];
     if (active) {
-      if (beta != 0.0f) {
-        float cin[G];
-        int64_t o = off;
-#pragma unroll
-        for (int r = 0; r < G; ++r, o += p.ldc)
-          if (g + r < rows) cin[r] = load_c(p, o);
-#pragma unroll
-        for (int r = 0; r < G; ++r) w[r] = fmaf(beta, cin[r], w[r]);
-      }
 #pragma unroll
       for (int r = 0; r < G; ++r, off += p.ldc)
         if (g + r < rows) store_c(p, off, w[r]);
