@@ -299,6 +299,60 @@ def time_e2e(p, steps, warmup, stream, dev):
     return ms, h2d, d2h
 
 
+def grouped_measure(dev, stream, steps, count=1000, seed=7):
+    """Many small independent products (M, N, K drawn from 64..256, bf16 in,
+    fp32 out): one grouped launch against one bmm_run per problem.  Both
+    are timed with CUDA events around the whole set on the same stream."""
+    import torch
+    from dense_matmul_tensor_gb300 import bmm
+    rng = np.random.default_rng(seed)
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    items, plans, flops = [], [], 0
+    for _ in range(count):
+        M, N, K = (int(rng.choice([64, 128, 192, 256])) for _ in range(3))
+        A = torch.randn(M * K, generator=g, device=dev).to(torch.bfloat16)
+        B = torch.randn(K * N, generator=g, device=dev).to(torch.bfloat16)
+        C = torch.empty(M * N, dtype=torch.float32, device=dev)
+        items.append(dict(M=M, N=N, K=K, lda=K, ldb=N, ldc=N, A=A, B=B, C=C, alpha=1.0, beta=0.0))
+        plans.append(bmm.Plan(bmm.make_desc(batch=1, M=M, N=N, K=K, lda=K, ldb=N, ldc=N, strideA=0,
+                                            strideB=0, strideC=0, typeA="bf16", typeC="f32")))
+        flops += 2 * M * N * K
+    arr, n = bmm.make_problems(items)
+    gplan = bmm.bmm_grouped_create(arr, n, 0, 0, "bf16", "f32")
+    torch.cuda.synchronize()
+
+    def grouped():
+        bmm.bmm_grouped_run(gplan, arr, stream)
+
+    def singles():
+        for it, pl in zip(items, plans):
+            pl.run(it["A"], it["B"], it["C"], 1.0, 0.0, stream)
+
+    out = {}
+    for name, fn in (("grouped", grouped), ("one_call_per_problem", singles)):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = max(3, min(steps, 20))
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        out[name] = {"ms": ms, "TFLOP/s": flops / (ms * 1e-3) / 1e12}
+    info = bmm.bmm_grouped_get_info(gplan)
+    bmm.bmm_grouped_destroy(gplan)
+    for pl in plans:
+        pl.close()
+    out.update({"workload": f"grouped_{count}_problems_64_to_256_bf16_f32", "problems": count,
+                "tiles": info["tiles"], "tile_n": info["tile_n"],
+                "speedup_vs_one_call_per_problem": out["one_call_per_problem"]["ms"] / out["grouped"]["ms"]})
+    return out
+
+
 def metric_value(p, ms):
     return p.flops() / (ms * 1e-3) / 1e12  # TFLOP/s
 
@@ -498,6 +552,7 @@ def main():
             del qa, qb, qc
             torch.cuda.empty_cache()
         line["other_workloads"] = other
+        line["grouped"] = grouped_measure(dev, stream, args.steps)
 
     if rank == 0 and not args.no_cpu:
         sampler = OracleSample(p)

@@ -25,7 +25,9 @@ BMM_ERR_DEVICE_TIMEOUT = 5
 BMM_ERR_NO_DEVICE = 6
 
 EXPORTED = ("bmm_create", "bmm_plan_query", "bmm_get_plan_info", "bmm_run",
-            "bmm_get_device_error", "bmm_destroy", "bmm_status_string", "bmm_version")
+            "bmm_get_device_error", "bmm_destroy", "bmm_status_string", "bmm_version",
+            "bmm_grouped_create", "bmm_grouped_run", "bmm_grouped_get_device_error",
+            "bmm_grouped_get_info", "bmm_grouped_destroy")
 
 
 class bmm_desc_t(ctypes.Structure):
@@ -218,3 +220,78 @@ def bmm_run_noalloc(desc: bmm_desc_t, A, B, C, alpha=1.0, beta=0.0, stream=None,
             _stream(stream), _ptr(device_error))
     if st != BMM_OK:
         raise BmmError(st, "bmm_run_noalloc")
+
+
+# ------------------------------------------------------------ grouped launch
+
+class bmm_group_problem_t(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int64) for n in ("M", "N", "K", "lda", "ldb", "ldc")] + \
+               [("A", ctypes.c_void_p), ("B", ctypes.c_void_p), ("C", ctypes.c_void_p),
+                ("alpha", ctypes.c_float), ("beta", ctypes.c_float)]
+
+
+def _grouped_lib():
+    lib = load_library()
+    if lib.bmm_grouped_create.argtypes is None:
+        vp, P = ctypes.c_void_p, ctypes.POINTER
+        i32 = ctypes.c_int32
+        lib.bmm_grouped_create.argtypes = [i32, P(bmm_group_problem_t), i32, i32, i32, i32, P(vp)]
+        lib.bmm_grouped_create.restype = ctypes.c_int
+        lib.bmm_grouped_run.argtypes = [vp, P(bmm_group_problem_t), vp]
+        lib.bmm_grouped_run.restype = ctypes.c_int
+        lib.bmm_grouped_get_device_error.argtypes = [vp, P(ctypes.c_uint32)]
+        lib.bmm_grouped_get_device_error.restype = ctypes.c_int
+        lib.bmm_grouped_get_info.argtypes = [vp, P(i32), P(ctypes.c_int64), P(i32)]
+        lib.bmm_grouped_get_info.restype = ctypes.c_int
+        lib.bmm_grouped_destroy.argtypes = [vp]
+        lib.bmm_grouped_destroy.restype = ctypes.c_int
+    return lib
+
+
+def make_problems(items) -> ctypes.Array:
+    """items: iterable of dicts with M, N, K, lda, ldb, ldc, A, B, C, alpha,
+    beta (A/B/C as device pointers or tensors)."""
+    items = list(items)
+    arr = (bmm_group_problem_t * max(len(items), 1))()
+    for i, it in enumerate(items):
+        arr[i] = bmm_group_problem_t(it["M"], it["N"], it["K"], it["lda"], it["ldb"], it["ldc"],
+                                     _ptr(it.get("A")), _ptr(it.get("B")), _ptr(it.get("C")),
+                                     float(it.get("alpha", 1.0)), float(it.get("beta", 0.0)))
+    return arr, len(items)
+
+
+def bmm_grouped_create(problems, count, transA=0, transB=0, typeAB="bf16", typeC="f32"):
+    plan = ctypes.c_void_p()
+    t = lambda v: DTYPES[v] if isinstance(v, str) else int(v)  # noqa: E731
+    st = _grouped_lib().bmm_grouped_create(int(count), problems, int(transA), int(transB), t(typeAB),
+                                           t(typeC), ctypes.byref(plan))
+    if st != BMM_OK:
+        raise BmmError(st, "bmm_grouped_create")
+    return plan
+
+
+def bmm_grouped_run(plan, problems, stream=None):
+    st = _grouped_lib().bmm_grouped_run(plan, problems, _stream(stream))
+    if st != BMM_OK:
+        raise BmmError(st, "bmm_grouped_run")
+
+
+def bmm_grouped_get_device_error(plan):
+    w = ctypes.c_uint32(0)
+    st = _grouped_lib().bmm_grouped_get_device_error(plan, ctypes.byref(w))
+    return st, w.value
+
+
+def bmm_grouped_get_info(plan):
+    tn, tiles, stages = ctypes.c_int32(), ctypes.c_int64(), ctypes.c_int32()
+    st = _grouped_lib().bmm_grouped_get_info(plan, ctypes.byref(tn), ctypes.byref(tiles),
+                                             ctypes.byref(stages))
+    if st != BMM_OK:
+        raise BmmError(st, "bmm_grouped_get_info")
+    return {"tile_n": tn.value, "tiles": tiles.value, "stages": stages.value}
+
+
+def bmm_grouped_destroy(plan):
+    st = _grouped_lib().bmm_grouped_destroy(plan)
+    if st != BMM_OK:
+        raise BmmError(st, "bmm_grouped_destroy")

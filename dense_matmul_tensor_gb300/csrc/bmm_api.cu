@@ -10,6 +10,7 @@
 #include <cstring>
 #include <mutex>
 #include <new>
+#include <vector>
 
 #include "../../include/bmm.h"
 #include "bmm_kernel.cuh"
@@ -670,3 +671,271 @@ extern "C" bmm_status_t bmm_run_noalloc(const bmm_desc_t* desc, const void* A, c
     return BMM_ERR_CUDA;
   return BMM_OK;
 }
+
+// ---------------------------------------------------------------------------
+// Grouped launches: one persistent launch over a table of independent
+// problems (see bmm.h).  The single-CTA kernel runs in its grouped mode: each
+// role looks its tile up in the device table (binary search over each
+// problem's first tile) and takes that problem's sizes, tensor maps and C.
+
+struct bmm_grouped_plan_s {
+  int32_t count;                       // problems given by the caller
+  std::vector<int32_t> live;           // indices of the problems with tiles
+  std::vector<bmm_group_problem_t> shape;
+  int32_t transA, transB, typeAB, typeC;
+  int bn, stages;
+  uint32_t stage_bytes, a_bytes, tx_bytes, idesc, tmem_cols;
+  int64_t smem_bytes, tiles;
+  int sms;
+  std::vector<dmt::GroupEntry> host;   // staging copy of the device table
+  dmt::GroupEntry* table;
+  uint32_t* err;
+  uint64_t timeout_ns;
+};
+
+namespace {
+
+constexpr int32_t kMaxGroups = 65536;
+
+// One operand of a grouped problem as a (cols, rows, 1) tensor map: K-major
+// with a (64 x box_rows) box, MN-major with (64 x 64) boxes.
+bool encode_group_operand(int32_t type, int64_t rows, int64_t cols, int64_t ld, int box_rows,
+                          int mn_major, const void* base, CUtensorMap* out) {
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows), 1};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld * 2),
+                           static_cast<cuuint64_t>(round_up(rows * ld * 2, 16))};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(dmt::kTileK),
+                       static_cast<cuuint32_t>(mn_major ? 64 : box_rows), 1u};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  return g_encode(out, type == BMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                  3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_group_c(int32_t typeC, int64_t M, int64_t N, int64_t ldc, void* C, CUtensorMap* out) {
+  const int64_t es = typeC == BMM_F32 ? 4 : 2;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M), 1};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(ldc * es),
+                           static_cast<cuuint64_t>(round_up(M * ldc * es, 16))};
+  cuuint32_t box[3] = {32u, 32u, 1u};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  return g_encode(out, es == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, C,
+                  dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  es == 4 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                  CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BN>
+bool prepare_grouped_kernel() {
+  static std::once_flag once;
+  static bool ok = false;
+  std::call_once(once, [] {
+    ok = cudaFuncSetAttribute(dmt::bmm_tc_kernel<BN, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(dmt::kSmemLimit)) == cudaSuccess;
+  });
+  return ok;
+}
+
+template <int BN>
+cudaError_t launch_grouped(const bmm_grouped_plan_s* pl, const KParams& kp, cudaStream_t stream) {
+  if (!prepare_grouped_kernel<BN>()) return cudaErrorInvalidValue;
+  const int64_t grid = pl->tiles < pl->sms ? pl->tiles : pl->sms;
+  CUtensorMap unused;
+  std::memset(&unused, 0, sizeof(unused));
+  dmt::bmm_tc_kernel<BN, true><<<static_cast<unsigned>(grid), dmt::kThreads,
+                                 static_cast<size_t>(pl->smem_bytes), stream>>>(kp, unused, unused, unused);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+extern "C" {
+
+bmm_status_t bmm_grouped_create(int32_t count, const bmm_group_problem_t* problems, int32_t transA,
+                                int32_t transB, int32_t typeAB, int32_t typeC,
+                                bmm_grouped_plan_t* out) {
+  if (!out) return BMM_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (count < 0 || (count > 0 && !problems)) return BMM_ERR_INVALID_ARG;
+  if (count > kMaxGroups) return BMM_ERR_UNSUPPORTED;
+  if ((transA != 0 && transA != 1) || (transB != 0 && transB != 1)) return BMM_ERR_INVALID_ARG;
+  if (!is16(typeAB) || (typeC != BMM_F32 && typeC != BMM_BF16)) return BMM_ERR_INVALID_ARG;
+  const int64_t ces = typeC == BMM_F32 ? 4 : 2;
+  int64_t max_n = 0;
+  for (int32_t i = 0; i < count; ++i) {
+    const bmm_group_problem_t& q = problems[i];
+    if (q.M < 0 || q.N < 0 || q.K < 0) return BMM_ERR_INVALID_ARG;
+    const int64_t a_cols = transA ? q.M : q.K, b_cols = transB ? q.K : q.N;
+    if (q.lda < (a_cols > 1 ? a_cols : 1) || q.ldb < (b_cols > 1 ? b_cols : 1) ||
+        q.ldc < (q.N > 1 ? q.N : 1))
+      return BMM_ERR_INVALID_ARG;
+    if (q.M > kMaxDim || q.N > kMaxDim || q.K > kMaxDim) return BMM_ERR_UNSUPPORTED;
+    if (q.M == 0 || q.N == 0) continue;
+    if (q.K == 0) return BMM_ERR_UNSUPPORTED;
+    if ((q.lda * 2) % 16 || (q.ldb * 2) % 16 || (q.ldc * ces) % 16) return BMM_ERR_UNSUPPORTED;
+    if (q.N > max_n) max_n = q.N;
+  }
+  int dev = 0, major = 0, minor = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return BMM_ERR_NO_DEVICE;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return BMM_ERR_NO_DEVICE;
+  if (major != 10 || minor != 3) return BMM_ERR_NO_DEVICE;
+  if (!get_encoder()) return BMM_ERR_CUDA;
+
+  bmm_grouped_plan_s* pl = new (std::nothrow) bmm_grouped_plan_s();
+  if (!pl) return BMM_ERR_CUDA;
+  pl->count = count;
+  pl->shape.assign(problems, problems + count);
+  pl->transA = transA;
+  pl->transB = transB;
+  pl->typeAB = typeAB;
+  pl->typeC = typeC;
+  pl->sms = sms;
+  pl->timeout_ns = wait_timeout_ns();
+  // One tile shape for the launch: the smallest of 64/128/256 covering the widest N.
+  pl->bn = max_n <= 64 ? 64 : (max_n <= 128 ? 128 : 256);
+  const int a_mn = transA ? 1 : 0, b_mn = transB ? 0 : 1;
+  pl->a_bytes = static_cast<uint32_t>(dmt::kTileM * dmt::kTileK * 2);
+  const uint32_t b_bytes = static_cast<uint32_t>(pl->bn * dmt::kTileK * 2);
+  pl->stage_bytes = static_cast<uint32_t>(round_up(pl->a_bytes + b_bytes, 1024));
+  pl->tx_bytes = pl->a_bytes + b_bytes;
+  const int64_t fixed = 1024 + dmt::kEpiBytes + dmt::kBarBytes;
+  pl->stages = static_cast<int>((dmt::kSmemLimit - fixed) / pl->stage_bytes);
+  if (pl->stages > 16) pl->stages = 16;
+  pl->smem_bytes = fixed + static_cast<int64_t>(pl->stages) * pl->stage_bytes;
+  uint32_t cols = 32;
+  while (cols < static_cast<uint32_t>(2 * pl->bn)) cols <<= 1;
+  pl->tmem_cols = cols;
+  const uint32_t fmt = typeAB == BMM_BF16 ? 1u : 0u;
+  pl->idesc = (1u << 4) | (fmt << 7) | (fmt << 10) | (static_cast<uint32_t>(a_mn) << 15) |
+              (static_cast<uint32_t>(b_mn) << 16) | (static_cast<uint32_t>(pl->bn >> 3) << 17) |
+              (static_cast<uint32_t>(dmt::kTileM >> 4) << 24);
+  pl->tiles = 0;
+  for (int32_t i = 0; i < count; ++i) {
+    const bmm_group_problem_t& q = problems[i];
+    if (q.M == 0 || q.N == 0) continue;
+    dmt::GroupEntry e;
+    std::memset(static_cast<void*>(&e), 0, sizeof(e));
+    e.Mv = static_cast<int32_t>(q.M);
+    e.Nv = static_cast<int32_t>(q.N);
+    e.num_m = static_cast<int32_t>((q.M + dmt::kTileM - 1) / dmt::kTileM);
+    e.num_n = static_cast<int32_t>((q.N + pl->bn - 1) / pl->bn);
+    e.k_blocks = static_cast<int32_t>((q.K + dmt::kTileK - 1) / dmt::kTileK);
+    const int64_t rem = q.K % dmt::kTileK;
+    e.tail_steps = rem == 0 ? dmt::kTileK / dmt::kUmmaK
+                            : static_cast<int32_t>((rem + dmt::kUmmaK - 1) / dmt::kUmmaK);
+    e.tile_begin = pl->tiles;
+    e.ldc = q.ldc;
+    pl->tiles += static_cast<int64_t>(e.num_m) * e.num_n;
+    pl->live.push_back(i);
+    pl->host.push_back(e);
+  }
+  const size_t table_bytes = sizeof(dmt::GroupEntry) * (pl->host.empty() ? 1 : pl->host.size());
+  if (cudaMalloc(reinterpret_cast<void**>(&pl->table), table_bytes) != cudaSuccess) {
+    delete pl;
+    return BMM_ERR_CUDA;
+  }
+  if (cudaMalloc(reinterpret_cast<void**>(&pl->err), 256) != cudaSuccess ||
+      cudaMemset(pl->err, 0, 256) != cudaSuccess) {
+    cudaFree(pl->table);
+    cudaFree(pl->err);
+    delete pl;
+    return BMM_ERR_CUDA;
+  }
+  *out = pl;
+  return BMM_OK;
+}
+
+bmm_status_t bmm_grouped_run(bmm_grouped_plan_t pl, const bmm_group_problem_t* problems,
+                             void* stream_v) {
+  if (!pl || (pl->count > 0 && !problems)) return BMM_ERR_INVALID_ARG;
+  if (pl->tiles == 0) return BMM_OK;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+  const int64_t ces = pl->typeC == BMM_F32 ? 4 : 2;
+  const int b_box = pl->bn;
+  for (size_t j = 0; j < pl->live.size(); ++j) {
+    const int32_t i = pl->live[j];
+    const bmm_group_problem_t& q = problems[i];
+    const bmm_group_problem_t& s = pl->shape[i];
+    if (q.M != s.M || q.N != s.N || q.K != s.K || q.lda != s.lda || q.ldb != s.ldb || q.ldc != s.ldc)
+      return BMM_ERR_INVALID_ARG;  // sizes are fixed at create
+    if (!q.A || !q.B || !q.C) return BMM_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(q.A) & 15u) || (reinterpret_cast<uintptr_t>(q.B) & 15u))
+      return BMM_ERR_MISALIGNED;
+    dmt::GroupEntry& e = pl->host[j];
+    const int64_t a_rows = pl->transA ? q.K : q.M, a_cols = pl->transA ? q.M : q.K;
+    const int64_t b_rows = pl->transB ? q.N : q.K, b_cols = pl->transB ? q.K : q.N;
+    if (!encode_group_operand(pl->typeAB, a_rows, a_cols, q.lda, dmt::kTileM, pl->transA ? 1 : 0, q.A,
+                              &e.map_a) ||
+        !encode_group_operand(pl->typeAB, b_rows, b_cols, q.ldb, b_box, pl->transB ? 0 : 1, q.B,
+                              &e.map_b))
+      return BMM_ERR_CUDA;
+    const bool c_ok = (reinterpret_cast<uintptr_t>(q.C) & 15u) == 0 && (q.N * ces) % 16 == 0;
+    e.c_tma = (q.beta == 0.0f && c_ok) ? 1 : 0;
+    if (e.c_tma && !encode_group_c(pl->typeC, q.M, q.N, q.ldc, q.C, &e.map_c)) return BMM_ERR_CUDA;
+    e.C = q.C;
+    e.alpha = q.alpha;
+    e.beta = q.beta;
+  }
+  // Pageable source: the copy is staged before this call returns, so the host
+  // table may be rewritten by the next run.
+  if (cudaMemcpyAsync(pl->table, pl->host.data(), sizeof(dmt::GroupEntry) * pl->host.size(),
+                      cudaMemcpyHostToDevice, stream) != cudaSuccess)
+    return BMM_ERR_CUDA;
+
+  KParams kp;
+  std::memset(&kp, 0, sizeof(kp));
+  kp.tiles = pl->tiles;
+  kp.a_mn = pl->transA ? 1 : 0;
+  kp.b_mn = pl->transB ? 0 : 1;
+  kp.stages = pl->stages;
+  kp.stage_bytes = pl->stage_bytes;
+  kp.a_bytes = pl->a_bytes;
+  kp.tx_bytes = pl->tx_bytes;
+  kp.idesc = pl->idesc;
+  kp.tmem_cols = pl->tmem_cols;
+  kp.c_bf16 = pl->typeC == BMM_BF16 ? 1 : 0;
+  kp.err = pl->err;
+  kp.timeout_ns = pl->timeout_ns;
+  kp.groups = pl->table;
+  kp.ngroups = static_cast<int32_t>(pl->host.size());
+  cudaError_t e;
+  switch (pl->bn) {
+    case 64: e = launch_grouped<64>(pl, kp, stream); break;
+    case 128: e = launch_grouped<128>(pl, kp, stream); break;
+    default: e = launch_grouped<256>(pl, kp, stream); break;
+  }
+  return e == cudaSuccess ? BMM_OK : BMM_ERR_CUDA;
+}
+
+bmm_status_t bmm_grouped_get_device_error(bmm_grouped_plan_t pl, uint32_t* detail) {
+  if (!pl) return BMM_ERR_INVALID_ARG;
+  uint32_t w = 0;
+  if (cudaMemcpy(&w, pl->err, sizeof(w), cudaMemcpyDeviceToHost) != cudaSuccess) return BMM_ERR_CUDA;
+  if (w != 0 && cudaMemset(pl->err, 0, sizeof(w)) != cudaSuccess) return BMM_ERR_CUDA;
+  if (detail) *detail = w;
+  return w == 0 ? BMM_OK : BMM_ERR_DEVICE_TIMEOUT;
+}
+
+bmm_status_t bmm_grouped_get_info(bmm_grouped_plan_t pl, int32_t* tile_n, int64_t* tiles,
+                                  int32_t* stages) {
+  if (!pl) return BMM_ERR_INVALID_ARG;
+  if (tile_n) *tile_n = pl->bn;
+  if (tiles) *tiles = pl->tiles;
+  if (stages) *stages = pl->stages;
+  return BMM_OK;
+}
+
+bmm_status_t bmm_grouped_destroy(bmm_grouped_plan_t pl) {
+  if (!pl) return BMM_OK;
+  bmm_status_t st = BMM_OK;
+  if (pl->table && cudaFree(pl->table) != cudaSuccess) st = BMM_ERR_CUDA;
+  if (pl->err && cudaFree(pl->err) != cudaSuccess) st = BMM_ERR_CUDA;
+  delete pl;
+  return st;
+}
+
+}  // extern "C"

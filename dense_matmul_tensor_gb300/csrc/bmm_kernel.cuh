@@ -67,6 +67,19 @@ enum WaitSite : uint32_t {
   kSiteTestStall = 5,
 };
 
+// One problem of a grouped launch: an entry of a device table built by the
+// host (tensor maps first, so each is 128-byte aligned).  tile_begin is the
+// launch-wide index of the problem's first tile.
+struct alignas(128) GroupEntry {
+  CUtensorMap map_a, map_b, map_c;
+  void* C;
+  int64_t tile_begin;
+  int64_t ldc;
+  int32_t Mv, Nv, k_blocks, tail_steps, num_m, num_n;
+  float alpha, beta;
+  int32_t c_tma;
+};
+
 struct KParams {
   int32_t Mv, Nv, K;       // MMA view: D (Mv x Nv) = opA (Mv x K) * opB (K x Nv)
   int32_t num_m, num_n;    // tiles per batch item
@@ -90,7 +103,21 @@ struct KParams {
   uint32_t* err;           // device error word
   uint64_t timeout_ns;     // bound on any single wait
   int32_t test_stall;      // 1: the MMA thread first waits on a barrier nothing completes
+  const GroupEntry* groups;// grouped launches: the problem table (device memory)
+  int32_t ngroups;
 };
+
+// What the epilogue needs about C, for the launch or for one grouped problem.
+struct EpiArgs {
+  void* C;
+  int64_t ldc;
+  int32_t Mv, Nv, c_bf16, c_trans, c_tma;
+  float alpha, beta;
+};
+
+__device__ __forceinline__ EpiArgs epi_args(const KParams& p) {
+  return EpiArgs{p.C, p.ldc, p.Mv, p.Nv, p.c_bf16, p.c_trans, p.c_tma, p.alpha, p.beta};
+}
 
 struct Abort {
   volatile uint32_t* flag;
@@ -178,25 +205,71 @@ __device__ __forceinline__ void issue_kblock(uint32_t d_tmem, uint32_t alo, uint
   }
 }
 
-__device__ __forceinline__ void decode_tile(int64_t t, const KParams& p, int& b, int& mb, int& nb) {
-  const int64_t per = static_cast<int64_t>(p.num_m) * p.num_n;
-  b = static_cast<int>(t / per);
-  const int r = static_cast<int>(t - static_cast<int64_t>(b) * per);
-  const int group = kGroupM * p.num_n;
+// Tile r of one (num_m x num_n) grid, in GROUP_M-row groups for L2 reuse.
+__device__ __forceinline__ void decode_mn(int r, int num_m, int num_n, int& mb, int& nb) {
+  const int group = kGroupM * num_n;
   const int gid = r / group;
   const int first_m = gid * kGroupM;
-  const int gsz = min(p.num_m - first_m, kGroupM);
+  const int gsz = min(num_m - first_m, kGroupM);
   const int rin = r - gid * group;
   mb = first_m + rin % gsz;
   nb = rin / gsz;
 }
 
-__device__ __forceinline__ float load_c(const KParams& p, int64_t off) {
+__device__ __forceinline__ void decode_tile(int64_t t, const KParams& p, int& b, int& mb, int& nb) {
+  const int64_t per = static_cast<int64_t>(p.num_m) * p.num_n;
+  b = static_cast<int>(t / per);
+  decode_mn(static_cast<int>(t - static_cast<int64_t>(b) * per), p.num_m, p.num_n, mb, nb);
+}
+
+// Everything a role needs about tile t: its place, its K extent and the
+// tensor maps of its operands (the launch's, or its grouped problem's).
+struct TileCtx {
+  int b, mb, nb, k_blocks, tail_steps;
+  const CUtensorMap* map_a;
+  const CUtensorMap* map_b;
+  const CUtensorMap* map_c;
+  const GroupEntry* g;
+};
+
+template <bool kGrouped>
+__device__ __forceinline__ TileCtx tile_ctx(int64_t t, const KParams& p, const CUtensorMap* tmA,
+                                            const CUtensorMap* tmB, const CUtensorMap* tmC) {
+  TileCtx c;
+  if constexpr (!kGrouped) {
+    decode_tile(t, p, c.b, c.mb, c.nb);
+    c.k_blocks = p.k_blocks;
+    c.tail_steps = p.tail_steps;
+    c.map_a = tmA;
+    c.map_b = tmB;
+    c.map_c = tmC;
+    c.g = nullptr;
+  } else {
+    int lo = 0, hi = p.ngroups - 1;  // last problem whose first tile is <= t
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (p.groups[mid].tile_begin <= t) lo = mid;
+      else hi = mid - 1;
+    }
+    const GroupEntry* g = p.groups + lo;
+    decode_mn(static_cast<int>(t - g->tile_begin), g->num_m, g->num_n, c.mb, c.nb);
+    c.b = 0;
+    c.k_blocks = g->k_blocks;
+    c.tail_steps = g->tail_steps;
+    c.map_a = &g->map_a;
+    c.map_b = &g->map_b;
+    c.map_c = &g->map_c;
+    c.g = g;
+  }
+  return c;
+}
+
+__device__ __forceinline__ float load_c(const EpiArgs& p, int64_t off) {
   if (p.c_bf16) return __bfloat162float(static_cast<const __nv_bfloat16*>(p.C)[off]);
   return static_cast<const float*>(p.C)[off];
 }
 
-__device__ __forceinline__ void store_c(const KParams& p, int64_t off, float v) {
+__device__ __forceinline__ void store_c(const EpiArgs& p, int64_t off, float v) {
   if (p.c_bf16)
     static_cast<__nv_bfloat16*>(p.C)[off] = __float2bfloat16_rn(v);
   else
@@ -210,7 +283,7 @@ __device__ __forceinline__ void store_c(const KParams& p, int64_t off, float v) 
 // the compiler can prove, so interleaving would serialise one memory latency
 // per row), while the live registers stay bounded.
 template <int CW>
-__device__ __forceinline__ void store_chunk(const KParams& p, float (&v)[CW], float* stg, int lane,
+__device__ __forceinline__ void store_chunk(const EpiArgs& p, float (&v)[CW], float* stg, int lane,
                                             int row0, int col0, int64_t cbase) {
   constexpr int G = 8;
   const float alpha = p.alpha, beta = p.beta;
@@ -288,7 +361,7 @@ __device__ __forceinline__ void store_chunk(const KParams& p, float (&v)[CW], fl
 // map's swizzle (128-byte rows for fp32, 64-byte rows for bf16), then one
 // lane stores the box; TMA clips rows and columns outside C.  Two buffers
 // per warp alternate, so a box is written while the previous one drains.
-__device__ __forceinline__ void store_chunk_tma(const KParams& p, const CUtensorMap* tmC,
+__device__ __forceinline__ void store_chunk_tma(const EpiArgs& p, const CUtensorMap* tmC,
                                                 float (&v)[32], uint8_t* box, uint32_t box_addr,
                                                 int lane, int row0, int col0, int b) {
   const float alpha = p.alpha;
@@ -324,7 +397,10 @@ __device__ __forceinline__ void store_chunk_tma(const KParams& p, const CUtensor
   }
 }
 
-template <int BN>
+// kGrouped: the launch covers a table of independent problems (p.groups):
+// every role maps its tile to a problem and takes that problem's sizes,
+// tensor maps and C from the table; otherwise one batched problem.
+template <int BN, bool kGrouped = false>
 __global__ void __launch_bounds__(kThreads, 1)
     bmm_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUtensorMap tmA,
                   const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmC) {
@@ -365,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0u;
     fence_barrier_init();
   }
-  if (warp == 0 && lane == 0) {
+  if (warp == 0 && lane == 0 && !kGrouped) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     if (p.c_tma) tma_prefetch_desc(&tmC);
@@ -386,11 +462,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t it = 0;
       bool ok = true;
       for (int64_t t = blockIdx.x; t < p.tiles && ok; t += gridDim.x) {
-        int b, mb, nb;
-        decode_tile(t, p, b, mb, nb);
-        const int m0 = mb * kTileM, n0 = nb * BN;
-        const int za = p.a_bcast ? 0 : b, zb = p.b_bcast ? 0 : b;
-        for (int kb = 0; kb < p.k_blocks; ++kb, ++it) {
+        const TileCtx tc = tile_ctx<kGrouped>(t, p, &tmA, &tmB, &tmC);
+        const int m0 = tc.mb * kTileM, n0 = tc.nb * BN;
+        const int za = p.a_bcast ? 0 : tc.b, zb = p.b_bcast ? 0 : tc.b;
+        for (int kb = 0; kb < tc.k_blocks; ++kb, ++it) {
           const uint32_t s = it % S, ph = (it / S) & 1u;
           if (!wait_bounded<true>(empty_bar(s), ph ^ 1u, ab, kSiteProducerEmpty)) {
             ok = false;
@@ -401,17 +476,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(full_bar(s), p.tx_bytes);
           const int k0 = kb * kTileK;
           if (!p.a_mn) {
-            tma_load_3d(a_dst, &tmA, full_bar(s), k0, m0, za);
+            tma_load_3d(a_dst, tc.map_a, full_bar(s), k0, m0, za);
           } else {
-            tma_load_3d(a_dst, &tmA, full_bar(s), m0, k0, za);
-            tma_load_3d(a_dst + 8192u, &tmA, full_bar(s), m0 + 64, k0, za);
+            tma_load_3d(a_dst, tc.map_a, full_bar(s), m0, k0, za);
+            tma_load_3d(a_dst + 8192u, tc.map_a, full_bar(s), m0 + 64, k0, za);
           }
           if (!p.b_mn) {
-            tma_load_3d(b_dst, &tmB, full_bar(s), k0, n0, zb);
+            tma_load_3d(b_dst, tc.map_b, full_bar(s), k0, n0, zb);
           } else {
 #pragma unroll
             for (int h = 0; h < BN / 64; ++h)
-              tma_load_3d(b_dst + 8192u * h, &tmB, full_bar(s), n0 + 64 * h, k0, zb);
+              tma_load_3d(b_dst + 8192u * h, tc.map_b, full_bar(s), n0 + 64 * h, k0, zb);
           }
         }
       }
@@ -441,7 +516,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + acc * BN;
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
+        int k_blocks = p.k_blocks, tail_steps = p.tail_steps;
+        if constexpr (kGrouped) {
+          const TileCtx tc = tile_ctx<true>(t, p, &tmA, &tmB, &tmC);
+          k_blocks = tc.k_blocks;
+          tail_steps = tc.tail_steps;
+        }
+        for (int kb = 0; kb < k_blocks; ++kb) {
           if (!wait_bounded<true>(full_bar(s), ph, ab, kSiteMmaFull)) {
             ok = false;
             break;
@@ -450,7 +531,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // slot are both async-proxy operations ordered by the barrier's
           // transaction count, and a fence inside the accumulation chain
           // stalls the tensor pipe.
-          const int nsteps = (kb == p.k_blocks - 1) ? p.tail_steps : kTileK / kUmmaK;
+          const int nsteps = (kb == k_blocks - 1) ? tail_steps : kTileK / kUmmaK;
           issue_kblock<false>(d_tmem, alo0 + s * sstep, blo0 + s * sstep, hi, hi, astep, bstep,
                               p.idesc, nsteps, kb == 0);
           tc_commit(empty_bar(s));  // slot is free once these MMAs have read it
@@ -483,8 +564,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       __syncwarp();
       tc_fence_after_sync();
-      int b, mb, nb;
-      decode_tile(t, p, b, mb, nb);
+      const TileCtx tc = tile_ctx<kGrouped>(t, p, &tmA, &tmB, &tmC);
+      const int b = tc.b, mb = tc.mb, nb = tc.nb;
+      EpiArgs ea = epi_args(p);
+      if constexpr (kGrouped) {
+        ea = EpiArgs{tc.g->C, tc.g->ldc, tc.g->Mv, tc.g->Nv, p.c_bf16, 0, tc.g->c_tma,
+                     tc.g->alpha, tc.g->beta};
+      }
       const int row0 = mb * kTileM + q * 32;
       const int64_t cbase = static_cast<int64_t>(b) * p.sC;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
@@ -495,7 +581,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(acce_bar(acc));
-        store_chunk<16>(p, v, stg, lane, row0, nb * BN, cbase);
+        store_chunk<16>(ea, v, stg, lane, row0, nb * BN, cbase);
       } else {
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
@@ -507,12 +593,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(acce_bar(acc));  // accumulator may be reused
           }
-          if (p.c_tma) {
+          if (ea.c_tma) {
             const uint32_t k = nbox++ & 1u;
-            store_chunk_tma(p, &tmC, v, boxes + k * kEpiBoxBytes, boxes_addr + k * kEpiBoxBytes,
-                            lane, row0, nb * BN + 32 * c, b);
+            store_chunk_tma(ea, tc.map_c, v, boxes + k * kEpiBoxBytes,
+                            boxes_addr + k * kEpiBoxBytes, lane, row0, nb * BN + 32 * c, b);
           } else {
-            store_chunk<32>(p, v, stg, lane, row0, nb * BN + 32 * c, cbase);
+            store_chunk<32>(ea, v, stg, lane, row0, nb * BN + 32 * c, cbase);
           }
         }
       }
@@ -720,10 +806,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (p.c_tma) {
           const uint32_t k = nbox++ & 1u;
-          store_chunk_tma(p, &tmC, v, boxes + k * kEpiBoxBytes, boxes_addr + k * kEpiBoxBytes,
-                          lane, row0, nb * BN + 32 * c, b);
+          store_chunk_tma(epi_args(p), &tmC, v, boxes + k * kEpiBoxBytes,
+                          boxes_addr + k * kEpiBoxBytes, lane, row0, nb * BN + 32 * c, b);
         } else {
-          store_chunk<32>(p, v, stg, lane, row0, nb * BN + 32 * c, cbase);
+          store_chunk<32>(epi_args(p), v, stg, lane, row0, nb * BN + 32 * c, cbase);
         }
       }
     }

@@ -165,6 +165,61 @@ BMM_API bmm_status_t bmm_get_device_error(bmm_plan_t plan, uint32_t* detail);
 BMM_API bmm_status_t bmm_destroy(bmm_plan_t plan);
 
 /*
+ * Grouped launch: many independent products C_i = alpha_i*op(A_i)*op(B_i) +
+ * beta_i*C_i of different sizes in one persistent launch ("Triton
+ * Optimization Reference (cuTile -> Triton)", section 8: grouping many small
+ * tensors into one launch instead of one launch each, applied here to the
+ * contraction).  Every problem shares transA/transB and the element types;
+ * each has its own sizes, row strides, pointers and scalars.  Sizes and
+ * strides follow bmm_desc_t with batch = 1.
+ */
+typedef struct {
+  int64_t M, N, K;
+  int64_t lda, ldb, ldc;  /* elements */
+  const void* A;
+  const void* B;
+  void* C;
+  float alpha, beta;
+} bmm_group_problem_t;
+
+typedef struct bmm_grouped_plan_s* bmm_grouped_plan_t;
+
+/*
+ * Plan a grouped launch over `count` problems (host array; the sizes and
+ * strides are fixed here, pointers and scalars are read again at each run).
+ * Requirements beyond bmm_create's: K >= 1, and lda, ldb, ldc multiples of
+ * 16 bytes (no staging copies in a grouped launch).  Problems with M or N of
+ * 0 are skipped.  Allocates the plan's device problem table and error word.
+ * Returns BMM_OK, BMM_ERR_INVALID_ARG, BMM_ERR_UNSUPPORTED (K = 0, stride not
+ * a 16-byte multiple, count beyond 65536), BMM_ERR_NO_DEVICE or BMM_ERR_CUDA.
+ */
+BMM_API bmm_status_t bmm_grouped_create(int32_t count, const bmm_group_problem_t* problems,
+                                        int32_t transA, int32_t transB, int32_t typeAB,
+                                        int32_t typeC, bmm_grouped_plan_t* plan);
+
+/*
+ * Enqueue the grouped launch on `stream`: `problems` (host array, same count
+ * and sizes as at bmm_grouped_create) supplies this run's pointers and
+ * alpha/beta.  The problem table is copied to the device on `stream` before
+ * the kernel; one run of a plan may be in flight at a time.  A and B need
+ * 16-byte-aligned base pointers (BMM_ERR_MISALIGNED otherwise).  Unlike
+ * bmm_run, alpha == 0 still reads A and B.  Device-side wait timeouts are
+ * read with bmm_grouped_get_device_error.
+ */
+BMM_API bmm_status_t bmm_grouped_run(bmm_grouped_plan_t plan, const bmm_group_problem_t* problems,
+                                     void* stream);
+
+/* As bmm_get_device_error, for a grouped plan. */
+BMM_API bmm_status_t bmm_grouped_get_device_error(bmm_grouped_plan_t plan, uint32_t* detail);
+
+/* Tile width, tiles and stages the grouped plan uses (NULL pointers allowed). */
+BMM_API bmm_status_t bmm_grouped_get_info(bmm_grouped_plan_t plan, int32_t* tile_n,
+                                          int64_t* tiles, int32_t* stages);
+
+/* Free the grouped plan's device table and error word (cudaFree). */
+BMM_API bmm_status_t bmm_grouped_destroy(bmm_grouped_plan_t plan);
+
+/*
  * bmm_run without any allocation, for callers that cannot call cudaMalloc:
  * code running under an allocator that owns the device's memory (a caching
  * pool, a fixed budget reserved up front) and latency-critical call paths

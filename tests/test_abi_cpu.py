@@ -167,3 +167,18 @@ def test_wave_balanced_tile_width(lib, monkeypatch):
     monkeypatch.setenv("DMT_BMM_TILE_N", "224")
     # MN-major B on a pair is loaded in 64-column boxes per CTA: 224 is not allowed
     assert api.bmm_plan_query(desc_for(wl.RAGGED)).tile_n == 256
+
+
+def test_grouped_create_validates_before_any_device_call(lib):
+    ok = dict(M=64, N=64, K=64, lda=64, ldb=64, ldc=64)
+    for bad, code in [(dict(M=-1), api.BMM_ERR_INVALID_ARG), (dict(lda=10), api.BMM_ERR_INVALID_ARG),
+                      (dict(K=0), api.BMM_ERR_UNSUPPORTED), (dict(ldb=66), api.BMM_ERR_UNSUPPORTED)]:
+        arr, n = api.make_problems([dict(ok, **bad)])
+        with pytest.raises(api.BmmError) as e:
+            api.bmm_grouped_create(arr, n, 0, 0, "bf16", "f32")
+        assert e.value.status == code, bad
+    arr, n = api.make_problems([ok])
+    with pytest.raises(api.BmmError) as e:
+        api.bmm_grouped_create(arr, n, 2, 0, "bf16", "f32")
+    assert e.value.status == api.BMM_ERR_INVALID_ARG
+    assert lib.bmm_grouped_destroy(None) == api.BMM_OK
