@@ -69,6 +69,8 @@ def _load():
     lib.oracle_bmm_sampled.restype = i32
     lib.oracle_attention_probs_bf16.argtypes = [i64, i64, i64, f64, vp, vp, vp, i32]
     lib.oracle_attention_probs_bf16.restype = i32
+    lib.oracle_attention_f64.argtypes = [i64, i64, i64, i64, f64, vp, vp, vp, vp, vp, i32]
+    lib.oracle_attention_f64.restype = i32
     lib.oracle_round_bf16.argtypes = [f64]
     lib.oracle_round_bf16.restype = ctypes.c_uint16
     lib.oracle_decode16.argtypes = [ctypes.c_uint16, i32]
@@ -160,6 +162,29 @@ def attention_probs_bf16(Q, Kmat, *, batch, L, D, alpha, threads=None):
     if rc != 0:
         raise ValueError(f"oracle_attention_probs_bf16 failed (code {rc})")
     return P
+
+
+def attention(Q, Kmat, V, *, batch, Lq, Lk, D, alpha, threads=None, want_bound=True):
+    """O = softmax(alpha * Q K^T) V in fp64 from dense bf16 bit arrays
+    (Q: [batch, Lq, D]; K, V: [batch, Lk, D]).  Returns (O, Bnd) float64
+    [batch, Lq, D] with Bnd = sum_c p_ic |V_cd| (None if not wanted)."""
+    lib = _load()
+    Q, Kmat, V = _bits(Q, "Q"), _bits(Kmat, "K"), _bits(V, "V")
+    O = np.empty((batch, Lq, D), dtype=np.float64)
+    bnd = np.empty((batch, Lq, D), dtype=np.float64) if want_bound else None
+    rc = lib.oracle_attention_f64(batch, Lq, Lk, D, float(alpha), _ptr(Q), _ptr(Kmat), _ptr(V),
+                                  _ptr(O), _ptr(bnd), int(threads or host_threads()))
+    if rc != 0:
+        raise ValueError(f"oracle_attention_f64 failed (code {rc})")
+    return O, bnd
+
+
+def attention_tolerance(o_ref, bnd):
+    """Acceptance bound for the fused attention path per element: the
+    probabilities are rounded to bf16 before the P.V product (relative error
+    2^-8 each, so at most 2^-8 * sum_c p_ic |V_cd| in total, plus the fp32
+    sums), and O is rounded to bf16 once (2^-8 * |O|)."""
+    return 2.0 ** -7 * bnd + 2.0 ** -8 * np.abs(o_ref) + 1e-6
 
 
 def round_bf16(x):

@@ -360,3 +360,86 @@ int oracle_attention_probs_bf16(int64_t batch, int64_t L, int64_t D, double alph
   }
   return rc;
 }
+
+/* ------------------------------------------------- fused attention */
+
+typedef struct {
+  const uint16_t *Q, *K, *V;
+  double *O, *Bnd;
+  int64_t Lq, Lk, D;
+  double alpha;
+  int64_t lo, hi; /* flat query rows (b*Lq + i) */
+  int rc;
+} orc_att_job;
+
+static void* orc_attention_worker(void* p) {
+  orc_att_job* j = (orc_att_job*)p;
+  const int64_t Lq = j->Lq, Lk = j->Lk, D = j->D;
+  double* s = (double*)malloc((size_t)(Lk > 0 ? Lk : 1) * sizeof(double));
+  double* q = (double*)malloc((size_t)(D > 0 ? D : 1) * sizeof(double));
+  if (!s || !q) { free(s); free(q); j->rc = ORC_ENOMEM; return NULL; }
+  for (int64_t r = j->lo; r < j->hi; ++r) {
+    const int64_t b = r / Lq, i = r % Lq;
+    for (int64_t k = 0; k < D; ++k) q[k] = orc_bf16_to_f64(j->Q[(b * Lq + i) * D + k]);
+    double mx = -INFINITY;
+    for (int64_t c = 0; c < Lk; ++c) {
+      double acc = 0.0;
+      for (int64_t k = 0; k < D; ++k) acc += q[k] * orc_bf16_to_f64(j->K[(b * Lk + c) * D + k]);
+      s[c] = j->alpha * acc;
+      if (s[c] > mx) mx = s[c];
+    }
+    double sum = 0.0;
+    for (int64_t c = 0; c < Lk; ++c) { s[c] = exp(s[c] - mx); sum += s[c]; }
+    for (int64_t d = 0; d < D; ++d) {
+      double acc = 0.0, bnd = 0.0;
+      for (int64_t c = 0; c < Lk; ++c) {
+        const double pv = (s[c] / sum) * orc_bf16_to_f64(j->V[(b * Lk + c) * D + d]);
+        acc += pv;
+        bnd += fabs(pv);
+      }
+      j->O[(b * Lq + i) * D + d] = acc;
+      if (j->Bnd) j->Bnd[(b * Lq + i) * D + d] = bnd;
+    }
+  }
+  free(s); free(q);
+  return NULL;
+}
+
+/*
+ * The attention-shaped contraction in one piece, from its definition:
+ *   O[b,i,:] = sum_c softmax_c(alpha * Q[b,i,:] . K[b,c,:]) * V[b,c,:]
+ * with the softmax over c in fp64 (row maximum subtracted before exp(), which
+ * leaves it unchanged).  Q: [batch][Lq][D], K and V: [batch][Lk][D], dense
+ * bf16 bits.  Writes O and Bnd[b,i,d] = sum_c p_ic * |V[b,c,d]| (the scale of
+ * the sum, for tolerances) as [batch][Lq][D] fp64; Bnd may be NULL.
+ */
+int oracle_attention_f64(int64_t batch, int64_t Lq, int64_t Lk, int64_t D, double alpha,
+                         const uint16_t* Q, const uint16_t* K, const uint16_t* V,
+                         double* O, double* Bnd, int nthreads) {
+  if (batch < 0 || Lq < 0 || Lk < 1 || D < 0 || !O) return ORC_EINVAL;
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > 256) nthreads = 256;
+  const int64_t rows = batch * Lq;
+  if (rows == 0) return ORC_OK;
+  pthread_t th[256];
+  int started[256];
+  orc_att_job jobs[256];
+  const int64_t per = (rows + nthreads - 1) / nthreads;
+  for (int t = nthreads - 1; t >= 0; --t) {
+    orc_att_job jb = {Q, K, V, O, Bnd, Lq, Lk, D, alpha, t * per < rows ? t * per : rows,
+                      (t + 1) * per < rows ? (t + 1) * per : rows, ORC_OK};
+    jobs[t] = jb;
+    started[t] = 0;
+    if (jobs[t].lo >= jobs[t].hi) continue;
+    if (t == 0 || pthread_create(&th[t], NULL, orc_attention_worker, &jobs[t]) != 0)
+      orc_attention_worker(&jobs[t]);
+    else
+      started[t] = 1;
+  }
+  int rc = ORC_OK;
+  for (int t = 0; t < nthreads; ++t) {
+    if (started[t]) pthread_join(th[t], NULL);
+    if (jobs[t].rc != ORC_OK) rc = jobs[t].rc;
+  }
+  return rc;
+}

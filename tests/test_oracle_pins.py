@@ -408,3 +408,66 @@ def test_pins_catch_planted_mistakes(name, tmp_path):
         # values near 1 in fp16 decode to twice their size: caught by the fp16 runs
         pass
     assert _pin_suite(mut) != [], f"pins did not catch mutation {name}"
+
+
+# ------------------------------------------------- fused attention oracle
+
+def _att_inputs(batch, Lq, Lk, D, seed):
+    Q = wl.bits16(batch * Lq * D, seed + 1, "normal", "bf16").reshape(batch, Lq, D)
+    Kt = wl.bits16(batch * Lk * D, seed + 2, "normal", "bf16").reshape(batch, Lk, D)
+    V = wl.bits16(batch * Lk * D, seed + 3, "normal", "bf16").reshape(batch, Lk, D)
+    return Q, Kt, V
+
+
+def test_attention_oracle_vs_library_softmax():
+    batch, Lq, Lk, D = 2, 33, 70, 16
+    Q, Kt, V = _att_inputs(batch, Lq, Lk, D, 500)
+    alpha = float(np.float32(1 / math.sqrt(D)))
+    O, bnd = oracle.attention(Q, Kt, V, batch=batch, Lq=Lq, Lk=Lk, D=D, alpha=alpha)
+    q, k, v = (torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).double() for x in (Q, Kt, V))
+    P = torch.softmax(alpha * (q @ k.transpose(1, 2)), dim=2)
+    ref = (P @ v).numpy()
+    absref = (P @ v.abs()).numpy()
+    assert np.all(np.abs(O - ref) <= 1e-12 * absref + 1e-300)
+    assert np.allclose(bnd, absref, rtol=1e-12, atol=0)
+
+
+def test_attention_oracle_closed_forms():
+    batch, Lq, Lk, D = 1, 5, 9, 8
+    _, Kt, V = _att_inputs(batch, Lq, Lk, D, 600)
+    # Q = 0: every score is 0, the softmax is uniform, O is the mean of V's rows
+    Q0 = np.zeros((batch, Lq, D), np.uint16)
+    O, _ = oracle.attention(Q0, Kt, V, batch=batch, Lq=Lq, Lk=Lk, D=D, alpha=1.0)
+    mean = oracle.decode(V, "bf16").mean(axis=1)
+    assert np.allclose(O, mean[:, None, :], rtol=0, atol=1e-15)
+    # one key aligned with the query and a huge scale: O is that key's value row
+    Qv = np.tile(encode(np.eye(D)[0] * 4.0, "bf16"), (batch, Lq, 1))
+    Kv = np.tile(encode(np.zeros(D), "bf16"), (batch, Lk, 1))
+    Kv[0, 6] = encode(np.eye(D)[0] * 4.0, "bf16")
+    O1, _ = oracle.attention(Qv, Kv, V, batch=batch, Lq=Lq, Lk=Lk, D=D, alpha=100.0)
+    assert np.allclose(O1[0], oracle.decode(V, "bf16")[0, 6][None, :], rtol=0, atol=1e-12)
+
+
+def test_attention_oracle_key_permutation_invariance():
+    batch, Lq, Lk, D = 1, 7, 12, 8
+    Q, Kt, V = _att_inputs(batch, Lq, Lk, D, 700)
+    perm = np.random.default_rng(3).permutation(Lk)
+    O, _ = oracle.attention(Q, Kt, V, batch=batch, Lq=Lq, Lk=Lk, D=D, alpha=0.3)
+    Op, _ = oracle.attention(Q, Kt[:, perm], V[:, perm], batch=batch, Lq=Lq, Lk=Lk, D=D, alpha=0.3)
+    assert np.allclose(O, Op, rtol=1e-13, atol=1e-15)
+
+
+def test_attention_oracle_matches_probs_then_product():
+    """The fused definition equals the two-step path of the pair workload
+    (probabilities from attention_probs, then their product with V) before
+    any rounding of P: compare with fp64 P from the library softmax."""
+    batch, L, D = 1, 40, 16
+    Q, Kt, V = _att_inputs(batch, L, L, D, 800)
+    alpha = 0.25
+    O, _ = oracle.attention(Q, Kt, V, batch=batch, Lq=L, Lk=L, D=D, alpha=alpha)
+    P = oracle.attention_probs_bf16(Q, Kt, batch=batch, L=L, D=D, alpha=alpha)
+    Pv = oracle.decode(P, "bf16")
+    Vv = oracle.decode(V, "bf16")
+    two_step = Pv @ Vv
+    bnd = np.abs(Pv) @ np.abs(Vv)
+    assert np.all(np.abs(O - two_step) <= 2.0 ** -8 * bnd + 1e-12)   # P rounded to bf16 once
