@@ -27,7 +27,8 @@ BMM_ERR_NO_DEVICE = 6
 EXPORTED = ("bmm_create", "bmm_plan_query", "bmm_get_plan_info", "bmm_run",
             "bmm_get_device_error", "bmm_destroy", "bmm_status_string", "bmm_version",
             "bmm_grouped_create", "bmm_grouped_run", "bmm_grouped_get_device_error",
-            "bmm_grouped_get_info", "bmm_grouped_destroy")
+            "bmm_grouped_get_info", "bmm_grouped_destroy",
+            "bmm_attn_create", "bmm_attn_run", "bmm_attn_get_device_error", "bmm_attn_destroy")
 
 
 class bmm_desc_t(ctypes.Structure):
@@ -295,3 +296,94 @@ def bmm_grouped_destroy(plan):
     st = _grouped_lib().bmm_grouped_destroy(plan)
     if st != BMM_OK:
         raise BmmError(st, "bmm_grouped_destroy")
+
+
+# ------------------------------------------------------------ fused attention
+
+class bmm_attn_desc_t(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int64) for n in ("batch", "Lq", "Lk", "D", "ldq", "ldk", "ldv", "ldo",
+                                              "strideQ", "strideK", "strideV", "strideO")] + \
+               [("alpha", ctypes.c_float)]
+
+
+def make_attn_desc(*, batch, Lq, Lk, D=128, alpha, ldq=None, ldk=None, ldv=None, ldo=None,
+                   strideQ=None, strideK=None, strideV=None, strideO=None) -> bmm_attn_desc_t:
+    """Descriptor of O = softmax(alpha Q K^T) V; dense strides by default."""
+    ldq, ldk, ldv, ldo = (x if x is not None else D for x in (ldq, ldk, ldv, ldo))
+    sq = strideQ if strideQ is not None else Lq * ldq
+    sk = strideK if strideK is not None else Lk * ldk
+    sv = strideV if strideV is not None else Lk * ldv
+    so = strideO if strideO is not None else Lq * ldo
+    return bmm_attn_desc_t(batch, Lq, Lk, D, ldq, ldk, ldv, ldo, sq, sk, sv, so, float(alpha))
+
+
+def _attn_lib():
+    lib = load_library()
+    if lib.bmm_attn_create.argtypes is None:
+        vp, P = ctypes.c_void_p, ctypes.POINTER
+        lib.bmm_attn_create.argtypes = [P(bmm_attn_desc_t), P(vp)]
+        lib.bmm_attn_create.restype = ctypes.c_int
+        lib.bmm_attn_run.argtypes = [vp, vp, vp, vp, vp, vp]
+        lib.bmm_attn_run.restype = ctypes.c_int
+        lib.bmm_attn_get_device_error.argtypes = [vp, P(ctypes.c_uint32)]
+        lib.bmm_attn_get_device_error.restype = ctypes.c_int
+        lib.bmm_attn_destroy.argtypes = [vp]
+        lib.bmm_attn_destroy.restype = ctypes.c_int
+    return lib
+
+
+def bmm_attn_create(desc: bmm_attn_desc_t):
+    plan = ctypes.c_void_p()
+    st = _attn_lib().bmm_attn_create(ctypes.byref(desc), ctypes.byref(plan))
+    if st != BMM_OK:
+        raise BmmError(st, "bmm_attn_create")
+    return plan
+
+
+def bmm_attn_run(plan, Q, K, V, O, stream=None):
+    st = _attn_lib().bmm_attn_run(plan, _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _stream(stream))
+    if st != BMM_OK:
+        raise BmmError(st, "bmm_attn_run")
+
+
+def bmm_attn_get_device_error(plan):
+    w = ctypes.c_uint32(0)
+    st = _attn_lib().bmm_attn_get_device_error(plan, ctypes.byref(w))
+    return st, w.value
+
+
+def bmm_attn_destroy(plan):
+    st = _attn_lib().bmm_attn_destroy(plan)
+    if st != BMM_OK:
+        raise BmmError(st, "bmm_attn_destroy")
+
+
+class AttnPlan:
+    """Owns one attention plan: ``with AttnPlan(desc) as p: p.run(Q, K, V, O, stream)``."""
+
+    def __init__(self, desc: bmm_attn_desc_t):
+        self.desc = desc
+        self.handle = bmm_attn_create(desc)
+
+    def run(self, Q, K, V, O, stream=None):
+        bmm_attn_run(self.handle, Q, K, V, O, stream)
+
+    def device_error(self):
+        return bmm_attn_get_device_error(self.handle)
+
+    def close(self):
+        if self.handle:
+            bmm_attn_destroy(self.handle)
+            self.handle = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

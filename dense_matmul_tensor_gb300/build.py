@@ -15,9 +15,10 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 LIBDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIBDIR, "libdmt_bmm.so")
-SOURCES = [os.path.join(CSRC, "bmm_api.cu")]
-DEPENDS = SOURCES + [os.path.join(CSRC, f) for f in ("bmm_kernel.cuh", "ptx.cuh")] + [
+SOURCES = [os.path.join(CSRC, "bmm_api.cu"), os.path.join(CSRC, "attn_api.cu")]
+DEPENDS = SOURCES + [os.path.join(CSRC, f) for f in ("bmm_kernel.cuh", "ptx.cuh", "attn_kernel.cuh")] + [
     os.path.join(ROOT, "include", "bmm.h")]
+OBJDIR = os.path.join(LIBDIR, "obj")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-DNDEBUG", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-shared",
@@ -31,7 +32,23 @@ def nvcc() -> str:
     return exe
 
 
+COMPILE = ["-O3", "-DNDEBUG", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
+           "-Xcompiler", "-fvisibility=hidden"]
+
+
+def compile_commands(extra=()) -> list:
+    """One nvcc command per translation unit (run in parallel)."""
+    return [[nvcc(), *ARCH, *COMPILE, *extra, "-I", os.path.join(ROOT, "include"), "-c", src, "-o",
+             os.path.join(OBJDIR, os.path.basename(src) + ".o")] for src in SOURCES]
+
+
+def link_command(out: str = LIB) -> list:
+    return [nvcc(), *ARCH, "-shared", "-o", out,
+            *[os.path.join(OBJDIR, os.path.basename(s) + ".o") for s in SOURCES]]
+
+
 def command(out: str = LIB, extra=()) -> list:
+    """Single-command form (compile and link every source in one nvcc call)."""
     return [nvcc(), *ARCH, *FLAGS, *extra, "-I", os.path.join(ROOT, "include"), "-o", out,
             *SOURCES]
 
@@ -45,30 +62,32 @@ def up_to_date() -> bool:
 
 def build(force: bool = False, verbose: bool = False) -> str:
     """Compile the library unless it is newer than every source; return its path."""
-    os.makedirs(LIBDIR, exist_ok=True)
-    if not force and up_to_date():
-        return LIB
-    tmp = LIB + f".tmp{os.getpid()}"
-    cmd = command(tmp)
-    if verbose:
-        print(" ".join(cmd), flush=True)
-    subprocess.run(cmd, check=True)
-    os.replace(tmp, LIB)
-    return LIB
+    return finish(start(force=force, verbose=verbose))
 
 
-def start(force: bool = False):
-    """Start the build in the background; returns a Popen or None if current."""
-    os.makedirs(LIBDIR, exist_ok=True)
+class _Build:
+    def __init__(self, procs, tmp):
+        self.procs, self.tmp = procs, tmp
+
+
+def start(force: bool = False, verbose: bool = False):
+    """Start compiling every translation unit in parallel; None if current."""
+    os.makedirs(OBJDIR, exist_ok=True)
     if not force and up_to_date():
         return None
-    return subprocess.Popen(command(LIB + f".tmp{os.getpid()}"))
+    procs = []
+    for cmd in compile_commands():
+        if verbose:
+            print(" ".join(cmd), flush=True)
+        procs.append(subprocess.Popen(cmd))
+    return _Build(procs, LIB + f".tmp{os.getpid()}")
 
 
-def finish(proc) -> str:
-    if proc is not None:
-        rc = proc.wait()
-        if rc != 0:
-            raise subprocess.CalledProcessError(rc, "nvcc")
-        os.replace(LIB + f".tmp{os.getpid()}", LIB)
+def finish(job) -> str:
+    if job is not None:
+        for p in job.procs:
+            if p.wait() != 0:
+                raise subprocess.CalledProcessError(p.returncode, "nvcc")
+        subprocess.run(link_command(job.tmp), check=True)
+        os.replace(job.tmp, LIB)
     return LIB

@@ -158,7 +158,7 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, Abor
 // Wait with a short fixed limit and no error report: before exit, lets this
 // CTA's own asynchronous copies and MMAs land (at once after a normal run;
 // bounded after an abort).
-__device__ __noinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+static __device__ __noinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 0; it < (1u << 24); ++it) {
     if (mbar_try_wait(bar, parity)) return;
@@ -829,7 +829,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Each thread moves one 8-element segment of a row: eight 2-byte loads (the
 // source rows need not be aligned) and one 16-byte store (destination rows
 // are).  Columns past the row end are written as zero; TMA never reads them.
-__global__ void pack16_kernel(const uint16_t* __restrict__ src, uint16_t* __restrict__ dst,
+static __global__ void pack16_kernel(const uint16_t* __restrict__ src, uint16_t* __restrict__ dst,
                               int64_t nb, int64_t rows, int64_t cols, int64_t ld_src,
                               int64_t s_src, int64_t ld_dst, int64_t s_dst) {
   const int64_t segs = (cols + 7) / 8;
@@ -854,7 +854,7 @@ __global__ void pack16_kernel(const uint16_t* __restrict__ src, uint16_t* __rest
 
 // C = beta * C (beta == 0 writes zeros without reading C): the alpha == 0 or
 // K == 0 case, where A and B are not read.
-__global__ void scale_c_kernel(void* C, int c_bf16, int64_t batch, int64_t M, int64_t N,
+static __global__ void scale_c_kernel(void* C, int c_bf16, int64_t batch, int64_t M, int64_t N,
                                int64_t ldc, int64_t sC, float beta) {
   const int64_t total_rows = batch * M;
   for (int64_t r = blockIdx.y; r < total_rows; r += gridDim.y) {

@@ -200,11 +200,12 @@ SKINNY = Problem(batch=1024, M=16, N=256, K=4096, type_ab="bf16", type_c="bf16",
 WORKLOADS = {p.name: p for p in (SMALL, GEMM_4096, RAGGED, ATTN_QK, ATTN_PV, SKINNY)}
 
 
-def attention_qkv(batch=128, L=2048, D=128):
-    """Q, K, V bit arrays [batch, L, D] (bf16 normal) for the attention pair."""
-    base = 1000 * ATTN_QK.seed
-    n = batch * L * D
-    Q = bits16(n, base + SEED_A, "normal", "bf16").reshape(batch, L, D)
-    Kt = bits16(n, base + SEED_B, "normal", "bf16").reshape(batch, L, D)
-    V = bits16(n, base + SEED_V, "normal", "bf16").reshape(batch, L, D)
+def attention_qkv(batch=128, L=2048, D=128, Lk=None, seed=None):
+    """Q [batch, L, D] and K, V [batch, Lk, D] bit arrays (bf16 normal; Lk = L
+    unless given) for the attention pair and its fused form."""
+    base = 1000 * (ATTN_QK.seed if seed is None else seed)
+    Lk = L if Lk is None else Lk
+    Q = bits16(batch * L * D, base + SEED_A, "normal", "bf16").reshape(batch, L, D)
+    Kt = bits16(batch * Lk * D, base + SEED_B, "normal", "bf16").reshape(batch, Lk, D)
+    V = bits16(batch * Lk * D, base + SEED_V, "normal", "bf16").reshape(batch, Lk, D)
     return Q, Kt, V

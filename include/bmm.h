@@ -220,6 +220,47 @@ BMM_API bmm_status_t bmm_grouped_get_info(bmm_grouped_plan_t plan, int32_t* tile
 BMM_API bmm_status_t bmm_grouped_destroy(bmm_grouped_plan_t plan);
 
 /*
+ * Fused attention-shaped contraction: O[b] = softmax(alpha * Q[b] K[b]^T) V[b]
+ * with the softmax over keys, computed in one pass without writing the score
+ * matrix (the attention pair of the pages is S = alpha Q K^T, P = softmax(S),
+ * O = P V; "Triton Optimization Reference (cuTile -> Triton)", attention-style
+ * contractions).  Q: [batch][Lq][D], K and V: [batch][Lk][D], O: [batch][Lq][D],
+ * all bf16, row-major with row strides ld* and batch strides stride*
+ * (elements).  The probabilities are rounded to bf16 before their product
+ * with V (as in the two-step pair); accumulation is fp32; O is rounded to
+ * bf16 once.  This build supports D = 128 only.
+ */
+typedef struct {
+  int64_t batch, Lq, Lk, D;
+  int64_t ldq, ldk, ldv, ldo;
+  int64_t strideQ, strideK, strideV, strideO;
+  float alpha;
+} bmm_attn_desc_t;
+
+typedef struct bmm_attn_plan_s* bmm_attn_plan_t;
+
+/*
+ * Validate and plan.  Requirements: D = 128; row strides >= D; every stride a
+ * multiple of 8 elements (16 bytes); Lk >= 1 when there are queries; Lq and Lk
+ * at most 2^30 and batch below 2^31 (else BMM_ERR_UNSUPPORTED).  Allocates
+ * the plan's device error word.  Returns BMM_OK, BMM_ERR_INVALID_ARG,
+ * BMM_ERR_UNSUPPORTED, BMM_ERR_NO_DEVICE or BMM_ERR_CUDA.
+ */
+BMM_API bmm_status_t bmm_attn_create(const bmm_attn_desc_t* desc, bmm_attn_plan_t* plan);
+
+/* Enqueue O = softmax(alpha Q K^T) V on `stream`.  All four base pointers must
+ * be 16-byte aligned (BMM_ERR_MISALIGNED).  Asynchronous; one run of a plan in
+ * flight at a time. */
+BMM_API bmm_status_t bmm_attn_run(bmm_attn_plan_t plan, const void* Q, const void* K, const void* V,
+                                  void* O, void* stream);
+
+/* As bmm_get_device_error, for an attention plan. */
+BMM_API bmm_status_t bmm_attn_get_device_error(bmm_attn_plan_t plan, uint32_t* detail);
+
+/* Free the plan (cudaFree of its error word). */
+BMM_API bmm_status_t bmm_attn_destroy(bmm_attn_plan_t plan);
+
+/*
  * bmm_run without any allocation, for callers that cannot call cudaMalloc:
  * code running under an allocator that owns the device's memory (a caching
  * pool, a fixed budget reserved up front) and latency-critical call paths

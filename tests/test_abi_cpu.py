@@ -182,3 +182,36 @@ def test_grouped_create_validates_before_any_device_call(lib):
         api.bmm_grouped_create(arr, n, 2, 0, "bf16", "f32")
     assert e.value.status == api.BMM_ERR_INVALID_ARG
     assert lib.bmm_grouped_destroy(None) == api.BMM_OK
+
+
+def _attn(**kw):
+    base = dict(batch=2, Lq=100, Lk=70, alpha=0.125)
+    base.update(kw)
+    return api.make_attn_desc(**base)
+
+
+@pytest.mark.parametrize("bad,code", [
+    (dict(Lq=-1), api.BMM_ERR_INVALID_ARG),
+    (dict(ldk=64), api.BMM_ERR_INVALID_ARG),            # row stride below D
+    (dict(alpha=float("nan")), api.BMM_ERR_INVALID_ARG),
+    (dict(strideO=99 * 128), api.BMM_ERR_INVALID_ARG),   # O batch items would overlap
+    (dict(D=64, ldq=64, ldk=64, ldv=64, ldo=64), api.BMM_ERR_UNSUPPORTED),
+    (dict(ldv=130), api.BMM_ERR_UNSUPPORTED),           # not a multiple of 16 bytes
+    (dict(Lk=0), api.BMM_ERR_UNSUPPORTED),              # softmax over no keys
+    (dict(Lq=2 ** 30 + 1), api.BMM_ERR_UNSUPPORTED),
+])
+def test_attention_create_validates_before_any_device_call(lib, bad, code):
+    with pytest.raises(api.BmmError) as e:
+        api.bmm_attn_create(_attn(**bad))
+    assert e.value.status == code, bad
+    assert lib.bmm_attn_destroy(None) == api.BMM_OK
+    assert lib.bmm_attn_run(None, None, None, None, None, None) == api.BMM_ERR_INVALID_ARG
+
+
+def test_attention_create_without_a_gpu_reports_no_device(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    with pytest.raises(api.BmmError) as e:
+        api.bmm_attn_create(_attn())
+    assert e.value.status == api.BMM_ERR_NO_DEVICE
