@@ -353,6 +353,52 @@ def grouped_measure(dev, stream, steps, count=1000, seed=7):
     return out
 
 
+def fused_attention_measure(dev, stream, steps, flush, pair_ms=None, batch=128, L=2048, D=128):
+    """O = softmax(alpha Q K^T) V in one launch (bf16 in and out, fp32
+    accumulate), on the attention pair's shape: CUDA events per step with the
+    L2 flushed before each.  ``pair_ms`` (the two products of the unfused pair,
+    timed separately) is reported beside it."""
+    import torch
+    from dense_matmul_tensor_gb300 import bmm
+    from dense_matmul_tensor_gb300 import workloads as wl
+    alpha = float(np.float32(1.0 / np.sqrt(D)))
+    g = torch.Generator(device=dev)
+    g.manual_seed(4000)
+    q, k, v = (torch.randn(batch * L * D, generator=g, device=dev).to(torch.bfloat16)
+               for _ in range(3))
+    o = torch.empty_like(q)
+    plan = bmm.AttnPlan(bmm.make_attn_desc(batch=batch, Lq=L, Lk=L, D=D, alpha=alpha))
+    for i in range(3):
+        flush.fill_(i & 0xFF)
+        plan.run(q, k, v, o, stream)
+    torch.cuda.synchronize()
+    reps = max(3, min(steps, 20))
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(reps)]
+    with torch.cuda.stream(stream):
+        for i in range(reps):
+            flush.fill_(i & 0xFF)
+            ev[i][0].record(stream)
+            plan.run(q, k, v, o, stream)
+            ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    st, word = plan.device_error()
+    plan.close()
+    if st != bmm.BMM_OK:
+        raise RuntimeError(f"device error {word:#x} in the fused attention")
+    ms = statistics.fmean(a.elapsed_time(b) for a, b in ev)
+    flops = 4.0 * batch * L * L * D
+    nbytes = 4.0 * batch * L * D * 2
+    out = {"workload": f"attn_fused_b{batch}_{L}x{L}x{D}_bf16", "ms": ms,
+           "TFLOP/s": flops / (ms * 1e-3) / 1e12, "GB/s": nbytes / (ms * 1e-3) / 1e9,
+           "exp2_per_s": batch * L * L / (ms * 1e-3),
+           "kernel": "attn_fwd_kernel", "launches_per_step": 1}
+    if pair_ms is not None:
+        out["pair_qk_plus_pv_ms"] = pair_ms
+        out["speedup_vs_pair"] = pair_ms / ms
+    return out
+
+
 def metric_value(p, ms):
     return p.flops() / (ms * 1e-3) / 1e12  # TFLOP/s
 
@@ -552,6 +598,12 @@ def main():
             del qa, qb, qc
             torch.cuda.empty_cache()
         line["other_workloads"] = other
+        pair = {e["workload"]: e["ms"] for e in other}
+        qk, pv = wl.ATTN_QK.name, wl.ATTN_PV.name
+        pair_ms = pair[qk] + pair[pv] if qk in pair and pv in pair else None
+        fa = fused_attention_measure(dev, stream, args.steps, flush, pair_ms)
+        fa["frac_bf16_peak"] = fa["TFLOP/s"] / peaks["bf16_tflops"]
+        line["fused_attention"] = fa
         line["grouped"] = grouped_measure(dev, stream, args.steps)
 
     if rank == 0 and not args.no_cpu:

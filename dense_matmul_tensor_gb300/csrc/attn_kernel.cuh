@@ -21,7 +21,8 @@
 //               contiguous index is the head dimension) into O[j%2].
 //   warps 2..5  softmax and accumulation, one query row per thread: row
 //               maximum, p = exp2(s*alpha*log2e - m) written to shared memory
-//               as bf16 in the swizzled K-major layout the MMA reads,
+//               as bf16 in the swizzled K-major layout the MMA reads (two P
+//               buffers, so block j's softmax overlaps block j-1's product),
 //               O = O * exp2(m_old - m_new) + O_j in registers, then O / l.
 #pragma once
 
@@ -35,11 +36,12 @@ constexpr int kAttnN = 128;   // keys per block
 constexpr int kAttnStages = 2;
 constexpr uint32_t kAttnHalf = 128u * 128u;             // one 64-column half: 16 KB
 constexpr uint32_t kAttnQBytes = 2u * kAttnHalf;         // 32 KB
-constexpr uint32_t kAttnPBytes = 2u * kAttnHalf;         // 32 KB
+constexpr uint32_t kAttnPBytes = 2u * kAttnHalf;         // 32 KB per P buffer (two buffers)
 constexpr uint32_t kAttnKVBytes = 4u * kAttnHalf;        // K and V halves: 64 KB
 constexpr uint32_t kAttnBarBytes = 256;
 constexpr uint32_t kAttnSmem =
-    1024 + kAttnQBytes + kAttnPBytes + kAttnStages * kAttnKVBytes + kAttnBarBytes;
+    1024 + kAttnQBytes + 2 * kAttnPBytes + kAttnStages * kAttnKVBytes + kAttnBarBytes;
+static_assert(kAttnSmem <= 232448, "shared memory per CTA");
 
 struct AttnParams {
   int32_t Lq, Lk;
@@ -61,57 +63,117 @@ __device__ __forceinline__ float fast_exp2(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float y;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(a), "f"(b), "f"(c));
+  return y;
+}
+__device__ __forceinline__ float min3(float a, float b, float c) {
+  float y;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(a), "f"(b), "f"(c));
+  return y;
+}
+// (d0, d1) = (a0, a1) * (b0, b1) + (c0, c1) as one paired fp32 instruction
+__device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float b0, float b1,
+                                     float c0, float c1) {
+  asm("{\n\t.reg .b64 a, b, c, d;\n\t"
+      "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\tmov.b64 c, {%6, %7};\n\t"
+      "fma.rn.f32x2 d, a, b, c;\n\tmov.b64 {%0, %1}, d;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+__device__ __forceinline__ void add2(float& d0, float& d1, float a0, float a1) {
+  asm("{\n\t.reg .b64 a, d;\n\t"
+      "mov.b64 a, {%2, %3};\n\tmov.b64 d, {%0, %1};\n\t"
+      "add.rn.f32x2 d, d, a;\n\tmov.b64 {%0, %1}, d;\n\t}"
+      : "+f"(d0), "+f"(d1)
+      : "f"(a0), "f"(a1));
+}
+
+// Largest (kMin: smallest) raw score of this thread's row in one S block over
+// the first `valid` keys (all 128 when the block is full).
+template <bool kMin>
+__device__ __forceinline__ float row_extreme(uint32_t taddr, int valid) {
+  const float init = kMin ? INFINITY : -INFINITY;
+  float a = init, b = init;
+#pragma unroll 1
+  for (int c = 0; c < 4; ++c) {
+    float v[32];
+    tmem_ld_32cols(taddr + 32u * c, v);
+    tmem_wait_ld();
+    if (valid < 128) {
+#pragma unroll
+      for (int e = 0; e < 32; ++e)
+        if (32 * c + e >= valid) v[e] = init;
+    }
+#pragma unroll
+    for (int e = 0; e < 32; e += 4) {
+      a = kMin ? min3(a, v[e], v[e + 1]) : max3(a, v[e], v[e + 1]);
+      b = kMin ? min3(b, v[e + 2], v[e + 3]) : max3(b, v[e + 2], v[e + 3]);
+    }
+  }
+  return kMin ? fminf(a, b) : fmaxf(a, b);
+}
 
 // Softmax of one S block for this thread's query row (warp-uniform control):
-// row maximum of alpha * log2(e) * s over the valid keys, the new running maximum m and its rescale
-// factor r = exp2(m_old - m_new), the probabilities written as bf16 into the
-// P tile (two 64-key halves, 128-byte rows, 16-byte chunks XOR-swizzled by
-// row % 8 as TMA's 128-byte swizzle would place them), and l = l * r + sum
-// of the rounded probabilities.  Releases the S buffer and marks P ready.
+// the block's largest alpha * log2(e) * s over the valid keys, the new running
+// maximum m and its rescale factor r = exp2(m_old - m_new), the probabilities
+// p = exp2(alpha log2(e) s - m_new) written as bf16 into the P buffer (two
+// 64-key halves, 128-byte rows, 16-byte chunks XOR-swizzled by row % 8 as
+// TMA's 128-byte swizzle would place them), and l = l * r + sum(p).  Releases
+// the S buffer and marks P ready.  P buffer g % 2 is reused once the product
+// of block g - 2 has read it.
 __device__ __forceinline__ bool softmax_block(const AttnParams& p, const Abort& ab, uint32_t s_full,
                                               uint32_t s_empty, uint32_t p_ready, uint32_t p_free,
                                               uint32_t g, uint32_t ph, uint32_t taddr,
-                                              uint8_t* p_tile, int row, int lane, int key0,
+                                              uint8_t* p_buf, int row, int lane, int key0,
                                               float& m, float& l, float& r) {
   int w = 1;
-  if (lane == 0) w = wait_bounded(s_full, ph, ab, kSiteEpiAccFull) ? 1 : 0;
+  if (lane == 0) w = wait_bounded<true>(s_full, ph, ab, kSiteEpiAccFull) ? 1 : 0;
   if (!__shfl_sync(0xffffffffu, w, 0)) return false;
   __syncwarp();
   tc_fence_after_sync();
-  float mx = -INFINITY;
-#pragma unroll 1
-  for (int c = 0; c < 4; ++c) {
-    float v[32];
-    tmem_ld_32cols(taddr + 32u * c, v);
-    tmem_wait_ld();
-#pragma unroll
-    for (int e = 0; e < 32; ++e)
-      if (key0 + 32 * c + e < p.Lk) mx = fmaxf(mx, v[e] * p.scale_log2);  // any sign of alpha
-  }
-  const float m_new = fmaxf(m, mx);
+  const int valid = p.Lk - key0 < 128 ? p.Lk - key0 : 128;
+  const float sc = p.scale_log2;
+  // at least one key is valid, so the block's extreme is finite
+  const float m_blk = sc >= 0.0f ? row_extreme<false>(taddr, valid) * sc
+                                 : row_extreme<true>(taddr, valid) * sc;
+  const float m_new = fmaxf(m, m_blk);
   r = fast_exp2(m - m_new);  // exp2(-inf) = 0 for the first block
-  if (g > 0) {  // the previous block's P must have been read by its MMA
-    if (lane == 0) w = wait_bounded(p_free, (g - 1) & 1u, ab, kSiteEpiAccFull) ? 1 : 0;
+  if (g >= 2) {  // the product of block g - 2 must have read this P buffer
+    if (lane == 0) w = wait_bounded<true>(p_free, ((g >> 1) & 1u) ^ 1u, ab, kSiteEpiAccFull) ? 1 : 0;
     if (!__shfl_sync(0xffffffffu, w, 0)) return false;
   }
-  float sum = 0.0f;
+  const float nm = -m_new;
+  float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f, s3 = 0.0f;
 #pragma unroll 1
   for (int c = 0; c < 4; ++c) {
     float v[32];
     tmem_ld_32cols(taddr + 32u * c, v);
     tmem_wait_ld();
-    uint8_t* prow = p_tile + (c >> 1) * kAttnHalf + row * 128;
+    uint8_t* prow = p_buf + (c >> 1) * kAttnHalf + row * 128;
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) {
+      fma2(v[e], v[e + 1], v[e], v[e + 1], sc, sc, nm, nm);
+      v[e] = fast_exp2(v[e]);
+      v[e + 1] = fast_exp2(v[e + 1]);
+    }
+    if (valid < 128) {
+#pragma unroll
+      for (int e = 0; e < 32; ++e)
+        if (32 * c + e >= valid) v[e] = 0.0f;
+    }
+#pragma unroll
+    for (int e = 0; e < 32; e += 4) {
+      add2(s0, s1, v[e], v[e + 1]);
+      add2(s2, s3, v[e + 2], v[e + 3]);
+    }
 #pragma unroll
     for (int k = 0; k < 4; ++k) {  // one 16-byte chunk: 8 keys
       uint32_t wds[4];
 #pragma unroll
       for (int e2 = 0; e2 < 4; ++e2) {
-        const int e = 8 * k + 2 * e2;
-        const int key = key0 + 32 * c + e;
-        const float p0 = key < p.Lk ? fast_exp2(fmaf(v[e], p.scale_log2, -m_new)) : 0.0f;
-        const float p1 = key + 1 < p.Lk ? fast_exp2(fmaf(v[e + 1], p.scale_log2, -m_new)) : 0.0f;
-        const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
-        sum += __low2float(h2) + __high2float(h2);  // the rounded values are what P V uses
+        const __nv_bfloat162 h2 = __floats2bfloat162_rn(v[8 * k + 2 * e2], v[8 * k + 2 * e2 + 1]);
         wds[e2] = *reinterpret_cast<const uint32_t*>(&h2);
       }
       const int chunk = (c & 1) * 4 + k;
@@ -126,7 +188,9 @@ __device__ __forceinline__ bool softmax_block(const AttnParams& p, const Abort& 
     mbar_arrive(s_empty);
     mbar_arrive(p_ready);
   }
-  l = l * r + sum;
+  // l sums the unrounded p: the bf16 rounding then perturbs only the
+  // numerator of O = (P V) / l, by at most 2^-8 sum_c p_c |V_c| / l
+  l = l * r + ((s0 + s1) + (s2 + s3));
   m = m_new;
   return true;
 }
@@ -137,7 +201,7 @@ __device__ __forceinline__ bool fold_block(const Abort& ab, uint32_t o_full, uin
                                            uint32_t ph, uint32_t taddr, int lane, float r,
                                            float (&o)[kAttnD]) {
   int w = 1;
-  if (lane == 0) w = wait_bounded(o_full, ph, ab, kSiteEpiAccFull) ? 1 : 0;
+  if (lane == 0) w = wait_bounded<true>(o_full, ph, ab, kSiteEpiAccFull) ? 1 : 0;
   if (!__shfl_sync(0xffffffffu, w, 0)) return false;
   __syncwarp();
   tc_fence_after_sync();
@@ -147,7 +211,8 @@ __device__ __forceinline__ bool fold_block(const Abort& ab, uint32_t o_full, uin
     tmem_ld_32cols(taddr + 32u * c, v);
     tmem_wait_ld();
 #pragma unroll
-    for (int e = 0; e < 32; ++e) o[32 * c + e] = fmaf(o[32 * c + e], r, v[e]);
+    for (int e = 0; e < 32; e += 2)
+      fma2(o[32 * c + e], o[32 * c + e + 1], o[32 * c + e], o[32 * c + e + 1], r, r, v[e], v[e + 1]);
   }
   tc_fence_before_sync();
   __syncwarp();
@@ -166,7 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t q_addr = sbase;
   uint8_t* p_tile = smem + kAttnQBytes;
   const uint32_t p_addr = sbase + kAttnQBytes;
-  const uint32_t kv_addr0 = p_addr + kAttnPBytes;
+  const uint32_t kv_addr0 = p_addr + 2 * kAttnPBytes;
   const uint32_t bar0 = kv_addr0 + kAttnStages * kAttnKVBytes;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + (bar0 - sbase) + 8u * 20u);
   volatile uint32_t* abort_flag = tmem_slot + 1;
@@ -177,10 +242,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto kv_empty = [&](uint32_t s) { return bar0 + 32 + 8 * s; };
   auto s_full = [&](uint32_t s) { return bar0 + 48 + 8 * s; };
   auto s_empty = [&](uint32_t s) { return bar0 + 64 + 8 * s; };
-  const uint32_t p_ready = bar0 + 80, p_free = bar0 + 88;
-  auto o_full = [&](uint32_t s) { return bar0 + 96 + 8 * s; };
-  auto o_empty = [&](uint32_t s) { return bar0 + 112 + 8 * s; };
-  const uint32_t drain_bar = bar0 + 128;
+  const uint32_t p_ready = bar0 + 80;
+  auto p_free = [&](uint32_t s) { return bar0 + 88 + 8 * s; };
+  auto o_full = [&](uint32_t s) { return bar0 + 104 + 8 * s; };
+  auto o_empty = [&](uint32_t s) { return bar0 + 120 + 8 * s; };
+  const uint32_t drain_bar = bar0 + 136;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -194,9 +260,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(s_empty(s), 4);
       mbar_init(o_full(s), 1);
       mbar_init(o_empty(s), 4);
+      mbar_init(p_free(s), 1);
     }
     mbar_init(p_ready, 4);
-    mbar_init(p_free, 1);
     mbar_init(drain_bar, 1);
     *abort_flag = 0u;
     fence_barrier_init();
@@ -295,11 +361,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
             const uint32_t poff = (ks >> 2) * (kAttnHalf >> 4) + (ks & 3) * 2;
-            tc_mma_f16(d_tmem, desc_join(p_lo + poff, hi_sw), desc_join(v_lo + ks * 128u, hi_sw),
-                       p.idesc_o, ks > 0 ? 1u : 0u);
+            tc_mma_f16(d_tmem, desc_join(p_lo + s * (kAttnPBytes >> 4) + poff, hi_sw),
+                       desc_join(v_lo + ks * 128u, hi_sw), p.idesc_o, ks > 0 ? 1u : 0u);
           }
           tc_commit(o_full(s));
-          tc_commit(p_free);
+          tc_commit(p_free(s));
           tc_commit(kv_empty(s));
         }
       }
@@ -325,8 +391,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t g = gk + j;
         const uint32_t s = g & 1u, ph = (g >> 1) & 1u;
         float r;
-        ok = softmax_block(p, ab, s_full(s), s_empty(s), p_ready, p_free, g, ph,
-                           tmem_base + lane_off + s * 128u, p_tile, row, lane, j * kAttnN, m, l, r);
+        ok = softmax_block(p, ab, s_full(s), s_empty(s), p_ready, p_free(s), g, ph,
+                           tmem_base + lane_off + s * 128u, p_tile + s * kAttnPBytes, row, lane,
+                           j * kAttnN, m, l, r);
         if (!ok) break;
         if (j > 0) ok = fold_block(ab, o_full((g - 1) & 1u), o_empty((g - 1) & 1u), ((g - 1) >> 1) & 1u,
                                    tmem_base + lane_off + 256u + ((g - 1) & 1u) * 128u, lane, r_pend, o);
