@@ -146,16 +146,18 @@ bmm_status_t bmm_attn_run(bmm_attn_plan_t pl, const void* Q, const void* K, cons
                                    static_cast<int>(dmt::kAttnSmem)) == cudaSuccess;
   });
   if (!attr_ok) return BMM_ERR_CUDA;
+  const int rows_per_item = dmt::kAttnM;
   dmt::AttnParams ap;
   std::memset(&ap, 0, sizeof(ap));
   ap.Lq = static_cast<int32_t>(d.Lq);
   ap.Lk = static_cast<int32_t>(d.Lk);
-  ap.q_tiles = static_cast<int32_t>((d.Lq + dmt::kAttnM - 1) / dmt::kAttnM);
+  ap.q_tiles = static_cast<int32_t>((d.Lq + rows_per_item - 1) / rows_per_item);
   ap.k_blocks = static_cast<int32_t>((d.Lk + dmt::kAttnN - 1) / dmt::kAttnN);
   ap.items = d.batch * ap.q_tiles;
   ap.scale_log2 = static_cast<float>(static_cast<double>(d.alpha) * 1.4426950408889634);
   // 128 x 128 x 16 MMAs, bf16 in, fp32 accumulate; B of O = P V is MN-major
-  const uint32_t base = (1u << 4) | (1u << 7) | (1u << 10) | (16u << 17) | (8u << 24);
+  const uint32_t base = (1u << 4) | (1u << 7) | (1u << 10) | (16u << 17) |
+                        (static_cast<uint32_t>(rows_per_item >> 4) << 24);
   ap.idesc_s = base;
   ap.idesc_o = base | (1u << 16);
   ap.O = static_cast<__nv_bfloat16*>(O);
@@ -165,7 +167,7 @@ bmm_status_t bmm_attn_run(bmm_attn_plan_t pl, const void* Q, const void* K, cons
   ap.timeout_ns = pl->timeout_ns;
   ap.test_stall = pl->test_stall;
   const int64_t grid = ap.items < pl->sms ? ap.items : pl->sms;
-  dmt::attn_fwd_kernel<<<static_cast<unsigned>(grid), dmt::kThreads, dmt::kAttnSmem,
+  dmt::attn_fwd_kernel<<<static_cast<unsigned>(grid), dmt::kAttnThreads, dmt::kAttnSmem,
                          static_cast<cudaStream_t>(stream_v)>>>(ap, pl->map[0], pl->map[1], pl->map[2]);
   return cudaGetLastError() == cudaSuccess ? BMM_OK : BMM_ERR_CUDA;
 }

@@ -122,7 +122,8 @@ def test_fused_attention_matches_oracle(batch, Lq, Lk):
 
 def test_persistent_ctas_carry_ring_phases_across_tiles():
     # 160 x 2 = 320 query tiles on at most 152 CTAs: each CTA runs two or three
-    # tiles of three key blocks, so every barrier ring wraps across tiles
+    # tiles of three key blocks, so every barrier ring (and both O buffers)
+    # wraps across tiles
     _need_gpu()
     Q, K, V = wl.attention_qkv(160, 130, D, Lk=260, seed=21)
     O = run_attn(Q, K, V, alpha=ALPHA)
