@@ -18,22 +18,29 @@
 //               behind K.  A K slot is refilled once its S MMAs are done, a V
 //               slot once its P V MMAs are done.
 //   warp 1      one lane issues tcgen05.mma: S_j = Q K_j^T (both operands
-//               K-major) into S[j%2], one block ahead of O += P_j V_j (V read
-//               MN-major: its rows are keys, the contiguous index is the head
-//               dimension) into the tile's O buffer (O[t%2] for tile t).
-//   warps 2..9  softmax: two warpgroups, one query row per thread in each;
-//               warpgroup w owns keys [64w, 64w+64) of every block and head
-//               columns [64w, 64w+64) of O.  Both read the whole S row for its
-//               maximum (so they agree on it without exchanging), then each
-//               writes p = exp2(s*alpha*log2e - m) for its 64 keys into P[j%2]
-//               as bf16 in the swizzled K-major layout the MMA reads.
+//               K-major) into S[j%2], two blocks ahead of O[j%2] += P_j V_j
+//               (V read MN-major: its rows are keys, the contiguous index is
+//               the head dimension): S_{j+2} goes out as soon as block j's
+//               softmax has read S_j, so a warpgroup finds its next S ready.
+//   warps 2..9  softmax: two warpgroups, one query row per thread in each.
+//               Warpgroup w takes the blocks j = w (mod 2) of every tile with
+//               its own S[w], P[w] and output accumulator O[w], running
+//               maximum m_w and sum l_w, so the two run staggered: one's
+//               exponentials overlap the other's reads and waits.  Each reads
+//               its S row, writes p = exp2(s*alpha*log2e - m_w) as bf16 into
+//               P[w] in the swizzled K-major layout the MMA reads.  At the end
+//               of a tile the two halves are merged,
+//                 O = (O_0 2^(m_0 - m) + O_1 2^(m_1 - m)) / (l_0 2^(m_0 - m) + l_1 2^(m_1 - m)),
+//               m = max(m_0, m_1): warpgroup 1 hands (m_1, l_1) to warpgroup
+//               0, which returns both coefficients, and each warpgroup stores
+//               64 of the row's 128 columns.
 //
-// Lazy rescale: m is the largest scaled score seen when O was last rescaled.
-// A block whose maximum exceeds m by more than 8 (in log2 units) first waits
-// for the previous P V product, multiplies the row's O (in Tensor Memory) and
-// l by exp2(m_old - m_new) and moves m; otherwise p = exp2(s - m) <= 2^8 and
-// nothing is rescaled.  The result is the same softmax: only the common
-// factor exp2(-m) of numerator and denominator differs.
+// Lazy rescale: m_w is the largest scaled score seen when O[w] was last
+// rescaled.  A block whose maximum exceeds m_w by more than 8 (in log2 units)
+// multiplies the row's O[w] (in Tensor Memory) and l_w by exp2(m_old - m_new)
+// and moves m_w; otherwise p = exp2(s - m_w) <= 2^8 and nothing is rescaled.
+// Either way the result is the same softmax: only the common factor of
+// numerator and denominator differs.
 #pragma once
 
 #include "bmm_kernel.cuh"
@@ -47,7 +54,7 @@ constexpr int kAttnThreads = 320;  // TMA warp, MMA warp, two softmax warpgroups
 constexpr uint32_t kAttnHalf = 128u * 128u;       // one 64-column half of 128 rows: 16 KB
 constexpr uint32_t kAttnTile = 2u * kAttnHalf;    // Q, P, K or V tile: 32 KB
 constexpr uint32_t kAttnBarBytes = 256;
-constexpr uint32_t kAttnXchBytes = 2u * 128u * 4u;  // per-row partial sums of both warpgroups
+constexpr uint32_t kAttnXchBytes = 2u * 128u * 4u;  // per row: (m_1, l_1), then the coefficients
 // Q, P[2], K[2], V[2]
 constexpr uint32_t kAttnSmem = 1024 + 7 * kAttnTile + kAttnBarBytes + kAttnXchBytes;
 static_assert(kAttnSmem <= 232448, "shared memory per CTA");
@@ -132,28 +139,65 @@ __device__ __forceinline__ float extreme32(const float (&v)[32], int valid, floa
 }
 
 // Largest alpha * log2(e) * s over the valid keys of this thread's row of an
-// S block (128 columns at taddr); the warpgroup's own 64 columns (at
-// own_col) are kept in `mine`.  kMin: alpha < 0, so the smallest raw score
-// gives the largest scaled one.
+// S block (128 columns at taddr); the first 64 scores stay in `v`.  kMin:
+// alpha < 0, so the smallest raw score gives the largest scaled one.
 template <bool kMin>
-__device__ __forceinline__ float row_max_scaled(uint32_t taddr, uint32_t own_col, int valid,
-                                                float sc, float (&mine)[2][32]) {
+__device__ __forceinline__ float row_max_scaled(uint32_t taddr, int valid, float sc,
+                                                float (&v)[2][32]) {
   float acc = kMin ? INFINITY : -INFINITY;
-#pragma unroll
-  for (int h = 0; h < 2; ++h) tmem_ld_32cols(taddr + own_col + 32u * h, mine[h]);
-  tmem_wait_ld();
-#pragma unroll
-  for (int h = 0; h < 2; ++h)
-    acc = extreme32<kMin>(mine[h], valid - static_cast<int>(own_col) - 32 * h, acc);
-  const uint32_t other = own_col ^ 64u;
-#pragma unroll 1
-  for (int h = 0; h < 2; ++h) {
-    float v[32];
-    tmem_ld_32cols(taddr + other + 32u * h, v);
+  {  // the second half first: it is read again later
+    float u[2][32];
+    tmem_ld_32cols(taddr + 64u, u[0]);
+    tmem_ld_32cols(taddr + 96u, u[1]);
     tmem_wait_ld();
-    acc = extreme32<kMin>(v, valid - static_cast<int>(other) - 32 * h, acc);
+    acc = extreme32<kMin>(u[0], valid - 64, acc);
+    acc = extreme32<kMin>(u[1], valid - 96, acc);
   }
+  tmem_ld_32cols(taddr, v[0]);
+  tmem_ld_32cols(taddr + 32u, v[1]);
+  tmem_wait_ld();
+  acc = extreme32<kMin>(v[0], valid, acc);
+  acc = extreme32<kMin>(v[1], valid - 32, acc);
   return acc * sc;  // at least one key of the block is valid: finite
+}
+
+// p = exp2(s * sc - m) for 32 keys of the row (key0 = their first index
+// within the block; keys from `valid` on are zero), summed into (s0..s3) and
+// written as bf16 into the row of P (128-byte rows, two 64-key halves 16 KB
+// apart, 16-byte chunks XOR-swizzled by row % 8 as TMA's 128-byte swizzle
+// places them).
+__device__ __forceinline__ void exp_chunk(float (&v)[32], int key0, int valid, float sc, float nm,
+                                          uint8_t* prow, int row, float& s0, float& s1, float& s2,
+                                          float& s3) {
+#pragma unroll
+  for (int e = 0; e < 32; e += 2) {
+    fma2(v[e], v[e + 1], v[e], v[e + 1], sc, sc, nm, nm);
+    v[e] = fast_exp2(v[e]);
+    v[e + 1] = fast_exp2(v[e + 1]);
+  }
+  if (valid < key0 + 32) {
+#pragma unroll
+    for (int e = 0; e < 32; ++e)
+      if (key0 + e >= valid) v[e] = 0.0f;
+  }
+#pragma unroll
+  for (int e = 0; e < 32; e += 4) {
+    add2(s0, s1, v[e], v[e + 1]);
+    add2(s2, s3, v[e + 2], v[e + 3]);
+  }
+  const int c = key0 >> 5;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {  // one 16-byte chunk: 8 keys
+    uint32_t wds[4];
+#pragma unroll
+    for (int e2 = 0; e2 < 4; ++e2) {
+      const __nv_bfloat162 h2 = __floats2bfloat162_rn(v[8 * k + 2 * e2], v[8 * k + 2 * e2 + 1]);
+      wds[e2] = *reinterpret_cast<const uint32_t*>(&h2);
+    }
+    const int chunk = (c & 1) * 4 + k;
+    *reinterpret_cast<uint4*>(prow + (c >> 1) * kAttnHalf + ((chunk ^ (row & 7)) << 4)) =
+        make_uint4(wds[0], wds[1], wds[2], wds[3]);
+  }
 }
 
 __global__ void __launch_bounds__(kAttnThreads, 1)
@@ -180,16 +224,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   auto k_empty = [&](uint32_t s) { return bar0 + 32 + 8 * s; };
   auto v_full = [&](uint32_t s) { return bar0 + 48 + 8 * s; };
   auto v_empty = [&](uint32_t s) { return bar0 + 64 + 8 * s; };
-  auto s_full = [&](uint32_t s) { return bar0 + 80 + 8 * s; };
-  auto s_empty = [&](uint32_t s) { return bar0 + 96 + 8 * s; };
-  const uint32_t p_ready = bar0 + 112;
-  auto p_free = [&](uint32_t s) { return bar0 + 120 + 8 * s; };  // the P V of a block is done
-  auto o_full = [&](uint32_t s) { return bar0 + 136 + 8 * s; };
-  auto o_empty = [&](uint32_t s) { return bar0 + 152 + 8 * s; };
-  const uint32_t xch_bar = bar0 + 168;   // both warpgroups' partial sums are written
-  const uint32_t xch_read = bar0 + 176;  // ... and read: the slots may take the next tile's
-  const uint32_t drain_bar = bar0 + 184;
-  constexpr uint32_t kSoftmaxWarps = 8;
+  // per warpgroup w: S[w], P[w] and O[w]
+  auto s_full = [&](uint32_t w) { return bar0 + 80 + 8 * w; };
+  auto s_empty = [&](uint32_t w) { return bar0 + 96 + 8 * w; };
+  auto p_ready = [&](uint32_t w) { return bar0 + 112 + 8 * w; };
+  auto p_free = [&](uint32_t w) { return bar0 + 128 + 8 * w; };  // its last P V is done
+  const uint32_t o_full = bar0 + 144;    // the tile's last P V is done
+  const uint32_t o_empty = bar0 + 152;   // both O buffers have been read
+  const uint32_t xch_up = bar0 + 160;    // warpgroup 1's (m, l) are in the slot
+  const uint32_t xch_down = bar0 + 168;  // warpgroup 0's merge coefficients are in the slot
+  const uint32_t drain_bar = bar0 + 176;
+  constexpr uint32_t kGroupWarps = 4;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -202,14 +247,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       mbar_init(v_full(s), 1);
       mbar_init(v_empty(s), 1);
       mbar_init(s_full(s), 1);
-      mbar_init(s_empty(s), kSoftmaxWarps);
+      mbar_init(s_empty(s), kGroupWarps);
+      mbar_init(p_ready(s), kGroupWarps);
       mbar_init(p_free(s), 1);
-      mbar_init(o_full(s), 1);
-      mbar_init(o_empty(s), kSoftmaxWarps);
     }
-    mbar_init(p_ready, kSoftmaxWarps);
-    mbar_init(xch_bar, kSoftmaxWarps);
-    mbar_init(xch_read, kSoftmaxWarps);
+    mbar_init(o_full, 1);
+    mbar_init(o_empty, 2 * kGroupWarps);
+    mbar_init(xch_up, kGroupWarps);
+    mbar_init(xch_down, kGroupWarps);
     mbar_init(drain_bar, 1);
     *abort_flag = 0u;
     fence_barrier_init();
@@ -278,55 +323,65 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       const uint32_t q_lo = desc_lo(q_addr, 16u);
       const uint32_t p_lo = desc_lo(p_addr, 16u);
       uint32_t gk = 0, gs = 0, ti = 0;  // P V blocks issued, S blocks issued, tiles
+      uint32_t us0 = 0, us1 = 0, up0 = 0, up1 = 0;  // uses of S[w] and P[w]
       bool ok = !p.test_stall || wait_bounded(drain_bar, 0u, ab, kSiteTestStall);
-      // S_g = Q K_g^T: k-steps 0..3 in the first 64-column halves, 4..7 in the second.
-      auto issue_s = [&](uint32_t g) -> bool {
-        const uint32_t s = g & 1u, ph = (g >> 1) & 1u;
-        if (!wait_bounded<true>(k_full(s), ph, ab, kSiteMmaFull)) return false;
-        if (!wait_bounded<true>(s_empty(s), ph ^ 1u, ab, kSiteMmaAccEmpty)) return false;
+      // S_j = Q K_j^T into S[j % 2]: k-steps 0..3 in the first 64-column
+      // halves, 4..7 in the second.
+      auto issue_s = [&](uint32_t w) -> bool {
+        const uint32_t ks_ = gs & 1u;
+        if (!wait_bounded<true>(k_full(ks_), (gs >> 1) & 1u, ab, kSiteMmaFull)) return false;
+        const uint32_t u = w ? us1 : us0;
+        if (!wait_bounded<true>(s_empty(w), (u & 1u) ^ 1u, ab, kSiteMmaAccEmpty)) return false;
         tc_fence_after_sync();
-        const uint32_t k_lo = desc_lo(k_addr + s * kAttnTile, 16u);
-        const uint32_t d_tmem = tmem_base + s * 128u;
+        const uint32_t k_lo = desc_lo(k_addr + ks_ * kAttnTile, 16u);
+        const uint32_t d_tmem = tmem_base + w * 128u;
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
           const uint32_t off = (ks >> 2) * (kAttnHalf >> 4) + (ks & 3) * 2;  // (bytes >> 4)
           tc_mma_f16(d_tmem, desc_join(q_lo + off, hi_sw), desc_join(k_lo + off, hi_sw), p.idesc_s,
                      ks > 0 ? 1u : 0u);
         }
-        tc_commit(s_full(s));
-        tc_commit(k_empty(s));
+        tc_commit(s_full(w));
+        tc_commit(k_empty(ks_));
+        if (w) ++us1; else ++us0;
+        ++gs;
         return true;
       };
       for (int64_t item = blockIdx.x; item < p.items && ok; item += gridDim.x, ++ti) {
-        const uint32_t ob = ti & 1u;
         if (!wait_bounded<true>(q_full, ti & 1u, ab, kSiteMmaFull)) break;
+        // S_0 and S_1 first; then S_{j+2} before P_j V_j
+        ok = issue_s(0u) && (nb < 2 || issue_s(1u));
+        if (ok && nb <= 2) tc_commit(q_empty);  // Q is free once every S of this tile is done
         for (int j = 0; j < nb && ok; ++j, ++gk) {
-          if (j == 0) ok = issue_s(gs++);
-          if (ok && j + 1 < nb) ok = issue_s(gs++);
-          if (!ok) break;
-          if (j + 1 == nb) tc_commit(q_empty);  // Q is free once every S of this tile is done
-          const uint32_t s = gk & 1u, ph = (gk >> 1) & 1u;
-          if (!wait_bounded<true>(p_ready, gk & 1u, ab, kSiteMmaFull) ||
-              (j == 0 && !wait_bounded<true>(o_empty(ob), ((ti >> 1) & 1u) ^ 1u, ab, kSiteMmaAccEmpty)) ||
-              !wait_bounded<true>(v_full(s), ph, ab, kSiteMmaFull)) {
+          const uint32_t w = static_cast<uint32_t>(j) & 1u;
+          if (j + 2 < nb) {
+            if (!(ok = issue_s(w))) break;
+            if (j + 3 == nb) tc_commit(q_empty);
+          }
+          const uint32_t vs = gk & 1u;
+          if (!wait_bounded<true>(p_ready(w), (w ? up1 : up0) & 1u, ab, kSiteMmaFull) ||
+              (j == 0 && !wait_bounded<true>(o_empty, (ti & 1u) ^ 1u, ab, kSiteMmaAccEmpty)) ||
+              !wait_bounded<true>(v_full(vs), (gk >> 1) & 1u, ab, kSiteMmaFull)) {
             ok = false;
             break;
           }
           tc_fence_after_sync();
-          // O += P_g V_g: P K-major over keys (two 64-key halves); V MN-major
+          // O[w] += P_j V_j: P K-major over keys (two 64-key halves); V MN-major
           // (64-column halves of the head dimension 16 KB apart, 8 key rows per
-          // 1024-byte group, 16 keys = 2048 bytes per k-step).
-          const uint32_t v_lo = desc_lo(v_addr + s * kAttnTile, kAttnHalf);
-          const uint32_t d_tmem = tmem_base + 256u + ob * 128u;
+          // 1024-byte group, 16 keys = 2048 bytes per k-step).  The tile's
+          // first block of each warpgroup starts its O[w] afresh.
+          const uint32_t v_lo = desc_lo(v_addr + vs * kAttnTile, kAttnHalf);
+          const uint32_t d_tmem = tmem_base + 256u + w * 128u;
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
             const uint32_t poff = (ks >> 2) * (kAttnHalf >> 4) + (ks & 3) * 2;
-            tc_mma_f16(d_tmem, desc_join(p_lo + s * (kAttnTile >> 4) + poff, hi_sw),
-                       desc_join(v_lo + ks * 128u, hi_sw), p.idesc_o, (j > 0 || ks > 0) ? 1u : 0u);
+            tc_mma_f16(d_tmem, desc_join(p_lo + w * (kAttnTile >> 4) + poff, hi_sw),
+                       desc_join(v_lo + ks * 128u, hi_sw), p.idesc_o, (j >= 2 || ks > 0) ? 1u : 0u);
           }
-          tc_commit(p_free(s));
-          tc_commit(v_empty(s));
-          if (j + 1 == nb) tc_commit(o_full(ob));
+          tc_commit(p_free(w));
+          tc_commit(v_empty(vs));
+          if (j + 1 == nb) tc_commit(o_full);
+          if (w) ++up1; else ++up0;
         }
       }
       tc_commit(drain_bar);
@@ -334,44 +389,35 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
   } else {
     // --------------------------------------------------------- softmax
-    const int wg = (warp - 2) >> 2;               // key half / O column half owned
+    const uint32_t wg = static_cast<uint32_t>(warp - 2) >> 2;  // blocks j = wg (mod 2)
     const int quad = warp & 3;                    // TMEM lane quarter this warp may access
     const int row = quad * 32 + lane;             // query row within the tile
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-    const uint32_t own_col = static_cast<uint32_t>(wg) * 64u;
+    const uint32_t s_col = lane_off + wg * 128u;           // S[wg]
+    const uint32_t o_col = lane_off + 256u + wg * 128u;    // O[wg]
+    uint8_t* prow = p_tile + wg * kAttnTile + row * 128;   // this row of P[wg]
     const float sc = p.scale_log2;
-    uint32_t g = 0, ti = 0;
+    uint32_t n = 0, ti = 0;  // blocks this warpgroup has done, tiles
     bool ok = true;
     for (int64_t item = blockIdx.x; item < p.items && ok; item += gridDim.x, ++ti) {
-      const uint32_t ob = ti & 1u;
-      const uint32_t o_col = 256u + ob * 128u + own_col;
       const int b = static_cast<int>(item / p.q_tiles);
       const int qi = static_cast<int>(item % p.q_tiles) * kAttnM + row;
-      float m = 0.0f, l = 0.0f;
-      for (int j = 0; j < nb; ++j, ++g) {
-        const uint32_t s = g & 1u, ph = (g >> 1) & 1u;
+      float m = -INFINITY, l = 0.0f;
+      for (int j = static_cast<int>(wg); j < nb; j += 2, ++n) {
         const int valid = p.Lk - j * kAttnN < 128 ? p.Lk - j * kAttnN : 128;
-        if (!(ok = warp_wait(s_full(s), ph, ab, kSiteEpiAccFull, lane))) break;
+        if (!(ok = warp_wait(s_full(wg), n & 1u, ab, kSiteEpiAccFull, lane))) break;
         tc_fence_after_sync();
-        float mine[2][32];
-        const uint32_t taddr = tmem_base + lane_off + s * 128u;
-        const float m_blk = sc >= 0.0f ? row_max_scaled<false>(taddr, own_col, valid, sc, mine)
-                                       : row_max_scaled<true>(taddr, own_col, valid, sc, mine);
-        // this S buffer is no longer needed: the next-but-one S may overwrite it
-        tc_fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(s_empty(s));
-        bool grow = false;
-        if (j == 0) {
-          m = m_blk;
-        } else {
-          grow = m_blk > m + kAttnRescaleLog2;
-        }
+        float v[2][32];
+        const float m_blk = sc >= 0.0f ? row_max_scaled<false>(tmem_base + s_col, valid, sc, v)
+                                       : row_max_scaled<true>(tmem_base + s_col, valid, sc, v);
+        // this warpgroup's previous product must be done: P[wg] is then free
+        // and O[wg] final until the next product
+        if (n > 0 && !(ok = warp_wait(p_free(wg), (n - 1) & 1u, ab, kSiteEpiAccFull, lane))) break;
+        const bool first = j < 2;
+        const bool grow = !first && m_blk > m + kAttnRescaleLog2;
+        if (first) m = m_blk;
         if (__any_sync(0xffffffffu, grow)) {
-          // rescale O and l by exp2(m_old - m_new) in the rows that need it,
-          // after the previous block's product has landed in O
-          const uint32_t h = g - 1;
-          if (!(ok = warp_wait(p_free(h & 1u), (h >> 1) & 1u, ab, kSiteEpiAccFull, lane))) break;
+          // rescale O[wg] and l by exp2(m_old - m_new) in the rows that need it
           tc_fence_after_sync();
           const float r = grow ? fast_exp2(m - m_blk) : 1.0f;
           if (grow) {
@@ -379,100 +425,102 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             m = m_blk;
           }
 #pragma unroll 1
-          for (int c = 0; c < 2; ++c) {
-            float v[32];
-            tmem_ld_32cols(tmem_base + lane_off + o_col + 32u * c, v);
+          for (int c = 0; c < 8; ++c) {
+            float o[16];
+            tmem_ld_16cols(tmem_base + o_col + 16u * c, o);
             tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 32; e += 2) fma2(v[e], v[e + 1], v[e], v[e + 1], r, r, 0.0f, 0.0f);
-            tmem_st_32cols(tmem_base + lane_off + o_col + 32u * c, v);
+            for (int e = 0; e < 16; e += 2) fma2(o[e], o[e + 1], o[e], o[e + 1], r, r, 0.0f, 0.0f);
+            tmem_st_16cols(tmem_base + o_col + 16u * c, o);
           }
           tmem_wait_st();
         }
-        if (g >= 2) {  // the product of block g - 2 must have read this P buffer
-          if (!(ok = warp_wait(p_free(s), ph ^ 1u, ab, kSiteEpiAccFull, lane))) break;
-        }
-        // p for this warpgroup's 64 keys, into its 16 KB half of P[s]
+        // p for the block's 128 keys, into P[wg]: the first 64 from registers,
+        // the rest read again from S[wg], which is then released
         const float nm = -m;
-        const int my_valid = valid - static_cast<int>(own_col);
         float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f, s3 = 0.0f;
-        uint8_t* prow = p_tile + s * kAttnTile + wg * kAttnHalf + row * 128;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          float (&v)[32] = mine[h];
-#pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            fma2(v[e], v[e + 1], v[e], v[e + 1], sc, sc, nm, nm);
-            v[e] = fast_exp2(v[e]);
-            v[e + 1] = fast_exp2(v[e + 1]);
-          }
-          if (my_valid < 64) {
-#pragma unroll
-            for (int e = 0; e < 32; ++e)
-              if (32 * h + e >= my_valid) v[e] = 0.0f;
-          }
-#pragma unroll
-          for (int e = 0; e < 32; e += 4) {
-            add2(s0, s1, v[e], v[e + 1]);
-            add2(s2, s3, v[e + 2], v[e + 3]);
-          }
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {  // one 16-byte chunk: 8 keys
-            uint32_t wds[4];
-#pragma unroll
-            for (int e2 = 0; e2 < 4; ++e2) {
-              const __nv_bfloat162 h2 = __floats2bfloat162_rn(v[8 * k + 2 * e2], v[8 * k + 2 * e2 + 1]);
-              wds[e2] = *reinterpret_cast<const uint32_t*>(&h2);
-            }
-            const int chunk = h * 4 + k;
-            *reinterpret_cast<uint4*>(prow + ((chunk ^ (row & 7)) << 4)) =
-                make_uint4(wds[0], wds[1], wds[2], wds[3]);
-          }
-        }
+        exp_chunk(v[0], 0, valid, sc, nm, prow, row, s0, s1, s2, s3);
+        exp_chunk(v[1], 32, valid, sc, nm, prow, row, s0, s1, s2, s3);
+        tmem_ld_32cols(tmem_base + s_col + 64u, v[0]);
+        tmem_ld_32cols(tmem_base + s_col + 96u, v[1]);
+        tmem_wait_ld();
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(s_empty(wg));  // the warpgroup's next S may overwrite it
+        exp_chunk(v[0], 64, valid, sc, nm, prow, row, s0, s1, s2, s3);
+        exp_chunk(v[1], 96, valid, sc, nm, prow, row, s0, s1, s2, s3);
         // l sums the unrounded p: the bf16 rounding then perturbs only the
         // numerator of O = (P V) / l, by at most 2^-8 sum_c p_c |V_c| / l
         l += (s0 + s1) + (s2 + s3);
         fence_proxy_async_shared();  // P is read by the tensor core (async proxy)
         tc_fence_before_sync();      // and any rescale of O precedes the next product
         __syncwarp();
-        if (lane == 0) mbar_arrive(p_ready);
+        if (lane == 0) mbar_arrive(p_ready(wg));
       }
       if (!ok) break;
-      // both warpgroups' partial sums of this row; then O / l for own columns
-      if (ti > 0 && !(ok = warp_wait(xch_read, (ti - 1) & 1u, ab, kSiteEpiAccFull, lane))) break;
-      xch[wg * 128 + row] = l;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(xch_bar);
-      if (!(ok = warp_wait(xch_bar, ti & 1u, ab, kSiteEpiAccFull, lane))) break;
-      const float l_all = l + xch[(wg ^ 1) * 128 + row];
-      __syncwarp();
-      if (lane == 0) mbar_arrive(xch_read);
-      if (!(ok = warp_wait(o_full(ob), (ti >> 1) & 1u, ab, kSiteEpiAccFull, lane))) break;
+      // merge: warpgroup 1 hands over (m_1, l_1); warpgroup 0 returns the
+      // coefficients c_w = 2^(m_w - m) / l of both halves
+      float* xa = xch;        // per row: m_1, then c_0
+      float* xb = xch + 128;  // per row: l_1, then c_1
+      const bool two = nb >= 2;  // warpgroup 1 had a block in this tile
+      float c0, c1;
+      if (wg == 1) {
+        xa[row] = m;
+        xb[row] = l;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(xch_up);
+        if (!(ok = warp_wait(xch_down, ti & 1u, ab, kSiteEpiAccFull, lane))) break;
+        c0 = xa[row];
+        c1 = xb[row];
+      } else {
+        if (!(ok = warp_wait(xch_up, ti & 1u, ab, kSiteEpiAccFull, lane))) break;
+        const float m1 = xa[row], l1 = xb[row];
+        const float mm = two ? fmaxf(m, m1) : m;
+        const float a0 = fast_exp2(m - mm);
+        const float a1 = two ? fast_exp2(m1 - mm) : 0.0f;
+        const float inv = 1.0f / (l * a0 + l1 * a1);
+        c0 = a0 * inv;
+        c1 = a1 * inv;
+        xa[row] = c0;
+        xb[row] = c1;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(xch_down);
+      }
+      if (!(ok = warp_wait(o_full, ti & 1u, ab, kSiteEpiAccFull, lane))) break;
       tc_fence_after_sync();
-      const float inv = 1.0f / l_all;
+      // this warpgroup's 64 columns of the row: c_0 O_0 + c_1 O_1
+      const uint32_t col0 = wg * 64u;
       __nv_bfloat16* dst =
-          p.O + static_cast<int64_t>(b) * p.so + static_cast<int64_t>(qi) * p.ldo + own_col;
+          p.O + static_cast<int64_t>(b) * p.so + static_cast<int64_t>(qi) * p.ldo + col0;
 #pragma unroll 1
-      for (int c = 0; c < 2; ++c) {
-        float v[32];
-        tmem_ld_32cols(tmem_base + lane_off + o_col + 32u * c, v);
+      for (int c = 0; c < 4; ++c) {
+        float o0[16], o1[16];
+        tmem_ld_16cols(tmem_base + lane_off + 256u + col0 + 16u * c, o0);
+        if (two) tmem_ld_16cols(tmem_base + lane_off + 384u + col0 + 16u * c, o1);
         tmem_wait_ld();
-        if (c == 1) {  // this O buffer may take the tile after next
+        if (c == 3) {  // both O buffers may take the next tile
           tc_fence_before_sync();
           __syncwarp();
-          if (lane == 0) mbar_arrive(o_empty(ob));
+          if (lane == 0) mbar_arrive(o_empty);
+        }
+        if (!two) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) o1[e] = 0.0f;
         }
         if (qi < p.Lq) {
 #pragma unroll
-          for (int d = 0; d < 32; d += 8) {
+          for (int d = 0; d < 16; d += 8) {
             uint32_t wds[4];
 #pragma unroll
             for (int e2 = 0; e2 < 4; ++e2) {
-              const __nv_bfloat162 h2 =
-                  __floats2bfloat162_rn(v[d + 2 * e2] * inv, v[d + 2 * e2 + 1] * inv);
+              const int e = d + 2 * e2;
+              float x0, x1;
+              fma2(x0, x1, o0[e], o0[e + 1], c0, c0, 0.0f, 0.0f);
+              fma2(x0, x1, o1[e], o1[e + 1], c1, c1, x0, x1);
+              const __nv_bfloat162 h2 = __floats2bfloat162_rn(x0, x1);
               wds[e2] = *reinterpret_cast<const uint32_t*>(&h2);
             }
-            *reinterpret_cast<uint4*>(dst + 32 * c + d) = make_uint4(wds[0], wds[1], wds[2], wds[3]);
+            *reinterpret_cast<uint4*>(dst + 16 * c + d) = make_uint4(wds[0], wds[1], wds[2], wds[3]);
           }
         }
       }
