@@ -52,21 +52,23 @@ RECIPE_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustai
 
 # DRAM traffic per launch of the dominant kernel from one ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum; profiles/ has the summary),
-# keyed by a hash of the kernel sources and the workload: reported only while
-# the sources are unchanged.
+# keyed by a hash of that kernel's sources and the workload: reported only
+# while those sources are unchanged.
 NCU_TRAFFIC = {
-    ("d8808b2f9b9223ff", "gemm_4096x4096x4096_tn_bf16"): 85147392 + 17099520,
 }
+
+# the sources each kernel family is built from
+GEMM_SOURCES = ("bmm_api.cu", "bmm_kernel.cuh", "ptx.cuh")
+ATTN_SOURCES = ("attn_api.cu", "attn_kernel.cuh", "bmm_kernel.cuh", "ptx.cuh")
 
 FLUSH_BYTES = 512 << 20
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(files=GEMM_SOURCES) -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "dense_matmul_tensor_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh")):
-            h.update(open(os.path.join(csrc, f), "rb").read())
+    for f in files:
+        h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -94,6 +96,9 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's batch count (small cases for profiling)")
+    ap.add_argument("--attn-only", type=int, default=None, metavar="BATCH",
+                    help="time only the fused attention kernel (L = 2048, D = 128) at this batch "
+                         "and print its entry (profiling)")
     return ap.parse_args()
 
 
@@ -353,7 +358,8 @@ def grouped_measure(dev, stream, steps, count=1000, seed=7):
     return out
 
 
-def fused_attention_measure(dev, stream, steps, flush, pair_ms=None, batch=128, L=2048, D=128):
+def fused_attention_measure(dev, stream, steps, flush, peaks, pair_ms=None, batch=128, L=2048,
+                            D=128):
     """O = softmax(alpha Q K^T) V in one launch (bf16 in and out, fp32
     accumulate), on the attention pair's shape: CUDA events per step with the
     L2 flushed before each.  ``pair_ms`` (the two products of the unfused pair,
@@ -389,9 +395,17 @@ def fused_attention_measure(dev, stream, steps, flush, pair_ms=None, batch=128, 
     ms = statistics.fmean(a.elapsed_time(b) for a, b in ev)
     flops = 4.0 * batch * L * L * D
     nbytes = 4.0 * batch * L * D * 2
-    out = {"workload": f"attn_fused_b{batch}_{L}x{L}x{D}_bf16", "ms": ms,
-           "TFLOP/s": flops / (ms * 1e-3) / 1e12, "GB/s": nbytes / (ms * 1e-3) / 1e9,
+    name = f"attn_fused_b{batch}_{L}x{L}x{D}_bf16"
+    tf = flops / (ms * 1e-3) / 1e12
+    # two products of 2 L^2 D flops per batch item against Q, K, V and O once
+    # each: about 1000 flops per byte, far right of the ridge: tensor bound
+    out = {"workload": name, "ms": ms, "TFLOP/s": tf, "GB/s": nbytes / (ms * 1e-3) / 1e9,
            "exp2_per_s": batch * L * L / (ms * 1e-3),
+           "roofline": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"],
+                        "unit": "TFLOP/s", "frac": tf / peaks["bf16_tflops"],
+                        "traffic": NCU_TRAFFIC.get((kernel_source_hash(ATTN_SOURCES), name)),
+                        "algorithmic_flops_per_launch": flops,
+                        "algorithmic_bytes_per_launch": nbytes},
            "kernel": "attn_fwd_kernel", "launches_per_step": 1}
     if pair_ms is not None:
         out["pair_qk_plus_pv_ms"] = pair_ms
@@ -515,6 +529,15 @@ def main():
         if world > 1:
             dist.barrier()
 
+    if args.attn_only is not None:
+        flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        peaks_now, _ = load_peaks()
+        entry = fused_attention_measure(dev, torch.cuda.current_stream(), args.steps, flush_buf,
+                                        peaks_now, batch=args.attn_only)
+        if rank == 0:
+            print(json.dumps(entry), flush=True)
+        return
+
     def max_over_ranks(x):
         return reduce_max(x, world, dev)
 
@@ -601,9 +624,8 @@ def main():
         pair = {e["workload"]: e["ms"] for e in other}
         qk, pv = wl.ATTN_QK.name, wl.ATTN_PV.name
         pair_ms = pair[qk] + pair[pv] if qk in pair and pv in pair else None
-        fa = fused_attention_measure(dev, stream, args.steps, flush, pair_ms)
-        fa["frac_bf16_peak"] = fa["TFLOP/s"] / peaks["bf16_tflops"]
-        line["fused_attention"] = fa
+        line["fused_attention"] = fused_attention_measure(dev, stream, args.steps, flush, peaks,
+                                                          pair_ms)
         line["grouped"] = grouped_measure(dev, stream, args.steps)
 
     if rank == 0 and not args.no_cpu:

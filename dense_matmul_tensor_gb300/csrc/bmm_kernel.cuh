@@ -391,7 +391,7 @@ __device__ __forceinline__ void store_chunk_tma(const EpiArgs& p, const CUtensor
   }
   fence_proxy_async_shared();
   __syncwarp();
-  if (lane == 0 && row0 < p.Mv && col0 < p.Nv) {  // boxes wholly outside C are skipped
+  if (lane == 0) {
     tma_store_3d(tmC, box_addr, col0, row0, b);
     bulk_commit_group();
   }
@@ -594,9 +594,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) mbar_arrive(acce_bar(acc));  // accumulator may be reused
           }
           if (ea.c_tma) {
-            const uint32_t k = nbox++ & 1u;
-            store_chunk_tma(ea, tc.map_c, v, boxes + k * kEpiBoxBytes,
-                            boxes_addr + k * kEpiBoxBytes, lane, row0, nb * BN + 32 * c, b);
+            // A box wholly outside C is skipped outright: it neither writes a
+            // box buffer nor takes a turn, so the buffer alternation matches
+            // the committed store groups that the read-wait counts.
+            if (row0 < ea.Mv && nb * BN + 32 * c < ea.Nv) {
+              const uint32_t k = nbox++ & 1u;
+              store_chunk_tma(ea, tc.map_c, v, boxes + k * kEpiBoxBytes,
+                              boxes_addr + k * kEpiBoxBytes, lane, row0, nb * BN + 32 * c, b);
+            }
           } else {
             store_chunk<32>(ea, v, stg, lane, row0, nb * BN + 32 * c, cbase);
           }
@@ -805,9 +810,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) mbar_arrive_cluster(acc ? acce_leader1 : acce_leader0);
         }
         if (p.c_tma) {
-          const uint32_t k = nbox++ & 1u;
-          store_chunk_tma(epi_args(p), &tmC, v, boxes + k * kEpiBoxBytes,
-                          boxes_addr + k * kEpiBoxBytes, lane, row0, nb * BN + 32 * c, b);
+          // skipped outright when wholly outside C (see the single-CTA kernel)
+          if (row0 < p.Mv && nb * BN + 32 * c < p.Nv) {
+            const uint32_t k = nbox++ & 1u;
+            store_chunk_tma(epi_args(p), &tmC, v, boxes + k * kEpiBoxBytes,
+                            boxes_addr + k * kEpiBoxBytes, lane, row0, nb * BN + 32 * c, b);
+          }
         } else {
           store_chunk<32>(epi_args(p), v, stg, lane, row0, nb * BN + 32 * c, cbase);
         }

@@ -121,6 +121,26 @@ def test_box_store_edges(N, tc):
     assert np.all(c[pad] == fill)
 
 
+@pytest.mark.parametrize("pair", ["0", "1"])
+@pytest.mark.parametrize("N,tc", [(4064, "bf16"), (4096, "f32"), (480, "f32")])
+def test_skipped_boxes_never_recycle_a_buffer_in_flight(N, tc, pair, monkeypatch):
+    """Tiles whose last columns lie past N: the epilogue skips the boxes wholly
+    outside C.  A skipped box must not take a turn of the two box buffers, or
+    the next box is written into the buffer the last real store is still
+    reading (that store then sends the skipped box's zeros).  Widths are
+    chosen so the last tile column has one or two real boxes followed by
+    skipped ones; K is short so the epilogue runs back to back, and the run is
+    repeated."""
+    monkeypatch.setenv("DMT_BMM_PAIR", pair)
+    p = wl.Problem(batch=2, M=512, N=N, K=64, transB=True, type_ab="bf16", type_c=tc,
+                   seed=84 + N)
+    x = wl.make_inputs(p)
+    for _ in range(3):
+        c, info = run_gpu(p, x)
+        assert info.tile_n in (192, 224, 256) and info.cta_pair == int(pair)
+        check_full(p, x, c)
+
+
 def test_padded_aligned_leading_dimensions():
     p = wl.Problem(batch=2, M=130, N=260, K=100, transB=True, type_ab="bf16", type_c="bf16",
                    lda=136, ldb=112, ldc=272, sA=136 * 130 + 8, seed=82)
