@@ -356,6 +356,45 @@ __device__ __forceinline__ void store_chunk(const EpiArgs& p, float (&v)[CW], fl
   __syncwarp();  // staging tile free for the next chunk
 }
 
+// Request C_in for one 32-column chunk of a warp's 32 rows of row-major C
+// (lane = column): the loads are in flight while the previous chunk is
+// stored, and the first chunk of a tile while its mainloop still runs.
+__device__ __forceinline__ void prefetch_cin(const EpiArgs& p, float (&cin)[32], int lane, int row0,
+                                             int col0, int64_t cbase) {
+  const int j = col0 + lane;
+  const bool active = j < p.Nv;
+  const int rows = min(32, p.Mv - row0);
+  int64_t o = cbase + static_cast<int64_t>(row0) * p.ldc + j;
+#pragma unroll
+  for (int r = 0; r < 32; ++r, o += p.ldc)
+    if (active && r < rows) cin[r] = load_c(p, o);
+}
+
+// store_chunk for row-major C with beta != 0 and C_in already requested.
+__device__ __forceinline__ void store_chunk_cin(const EpiArgs& p, float (&v)[32], const float (&cin)[32],
+                                                float* stg, int lane, int row0, int col0,
+                                                int64_t cbase) {
+  constexpr int G = 8;
+  const float alpha = p.alpha, beta = p.beta;
+#pragma unroll
+  for (int r = 0; r < 32; ++r) stg[lane * kEpiPitch + r] = alpha * v[r];
+  __syncwarp();
+  const int j = col0 + lane;
+  const bool active = j < p.Nv;
+  const int rows = min(32, p.Mv - row0);
+  int64_t off = cbase + static_cast<int64_t>(row0) * p.ldc + j;
+#pragma unroll
+  for (int g = 0; g < 32; g += G) {
+    float w[G];
+#pragma unroll
+    for (int r = 0; r < G; ++r) w[r] = fmaf(beta, cin[g + r], stg[(g + r) * kEpiPitch + lane]);
+#pragma unroll
+    for (int r = 0; r < G; ++r, off += p.ldc)
+      if (active && g + r < rows) store_c(p, off, w[r]);
+  }
+  __syncwarp();  // staging tile free for the next chunk
+}
+
 // One chunk of 32 accumulator columns -> C through a TMA box store.  The
 // warp writes its 32 rows into a 4 KB box buffer laid out with the tensor
 // map's swizzle (128-byte rows for fp32, 64-byte rows for bf16), then one
@@ -558,12 +597,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t tl = 0;
     for (int64_t t = blockIdx.x; t < p.tiles; t += gridDim.x, ++tl) {
       const uint32_t acc = tl & 1u, aph = (tl >> 1) & 1u;
-      int ok = 1;
-      if (lane == 0) ok = wait_bounded(accf_bar(acc), aph, ab, kSiteEpiAccFull) ? 1 : 0;
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
-      __syncwarp();
-      tc_fence_after_sync();
       const TileCtx tc = tile_ctx<kGrouped>(t, p, &tmA, &tmB, &tmC);
       const int b = tc.b, mb = tc.mb, nb = tc.nb;
       EpiArgs ea = epi_args(p);
@@ -573,6 +606,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const int row0 = mb * kTileM + q * 32;
       const int64_t cbase = static_cast<int64_t>(b) * p.sC;
+      // row-major C with beta != 0 on the direct path: C_in two chunks deep,
+      // the first chunk requested before the accumulator is ready
+      const bool pre = BN >= 128 && ea.beta != 0.0f && !ea.c_tma && !ea.c_trans;
+      float cin[32];
+      if (pre) prefetch_cin(ea, cin, lane, row0, nb * BN, cbase);
+      int ok = 1;
+      if (lane == 0) ok = wait_bounded(accf_bar(acc), aph, ab, kSiteEpiAccFull) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      __syncwarp();
+      tc_fence_after_sync();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
       if constexpr (BN == 16) {
         float v[16];
@@ -602,6 +646,12 @@ __global__ void __launch_bounds__(kThreads, 1)
               store_chunk_tma(ea, tc.map_c, v, boxes + k * kEpiBoxBytes,
                               boxes_addr + k * kEpiBoxBytes, lane, row0, nb * BN + 32 * c, b);
             }
+          } else if (pre) {
+            float nxt[32];
+            if (c + 1 < BN / 32) prefetch_cin(ea, nxt, lane, row0, nb * BN + 32 * (c + 1), cbase);
+            store_chunk_cin(ea, v, cin, stg, lane, row0, nb * BN + 32 * c, cbase);
+#pragma unroll
+            for (int r = 0; r < 32; ++r) cin[r] = nxt[r];
           } else {
             store_chunk<32>(ea, v, stg, lane, row0, nb * BN + 32 * c, cbase);
           }
@@ -786,18 +836,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t acce_leader0 = mapa_shared(acce_bar(0), 0);
     const uint32_t acce_leader1 = mapa_shared(acce_bar(1), 0);
     uint32_t tl = 0;
+    const EpiArgs ea = epi_args(p);
+    // row-major C with beta != 0 on the direct path: C_in two chunks deep
+    const bool pre = p.beta != 0.0f && !p.c_tma && !p.c_trans;
     for (int64_t t = pair; t < p.tiles; t += npairs, ++tl) {
       const uint32_t acc = tl & 1u, aph = (tl >> 1) & 1u;
+      int b, mb, nb;
+      decode_tile(t, p, b, mb, nb);
+      const int row0 = mb * (2 * kTileM) + static_cast<int>(rank) * kTileM + q * 32;
+      const int64_t cbase = static_cast<int64_t>(b) * p.sC;
+      float cin[32];
+      if (pre) prefetch_cin(ea, cin, lane, row0, nb * BN, cbase);
       int ok = 1;
       if (lane == 0) ok = wait_bounded(accf_bar(acc), aph, ab, kSiteEpiAccFull) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       __syncwarp();
       tc_fence_after_sync();
-      int b, mb, nb;
-      decode_tile(t, p, b, mb, nb);
-      const int row0 = mb * (2 * kTileM) + static_cast<int>(rank) * kTileM + q * 32;
-      const int64_t cbase = static_cast<int64_t>(b) * p.sC;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
@@ -816,8 +871,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             store_chunk_tma(epi_args(p), &tmC, v, boxes + k * kEpiBoxBytes,
                             boxes_addr + k * kEpiBoxBytes, lane, row0, nb * BN + 32 * c, b);
           }
+        } else if (pre) {
+          float nxt[32];
+          if (c + 1 < BN / 32) prefetch_cin(ea, nxt, lane, row0, nb * BN + 32 * (c + 1), cbase);
+          store_chunk_cin(ea, v, cin, stg, lane, row0, nb * BN + 32 * c, cbase);
+#pragma unroll
+          for (int r = 0; r < 32; ++r) cin[r] = nxt[r];
         } else {
-          store_chunk<32>(epi_args(p), v, stg, lane, row0, nb * BN + 32 * c, cbase);
+          store_chunk<32>(ea, v, stg, lane, row0, nb * BN + 32 * c, cbase);
         }
       }
     }
