@@ -146,7 +146,7 @@ bmm_status_t bmm_attn_run(bmm_attn_plan_t pl, const void* Q, const void* K, cons
                                    static_cast<int>(dmt::kAttnSmem)) == cudaSuccess;
   });
   if (!attr_ok) return BMM_ERR_CUDA;
-  const int rows_per_item = dmt::kAttnM;
+  const int rows_per_item = dmt::kAttnItemRows;
   dmt::AttnParams ap;
   std::memset(&ap, 0, sizeof(ap));
   ap.Lq = static_cast<int32_t>(d.Lq);
@@ -157,7 +157,7 @@ bmm_status_t bmm_attn_run(bmm_attn_plan_t pl, const void* Q, const void* K, cons
   ap.scale_log2 = static_cast<float>(static_cast<double>(d.alpha) * 1.4426950408889634);
   // 128 x 128 x 16 MMAs, bf16 in, fp32 accumulate; B of O = P V is MN-major
   const uint32_t base = (1u << 4) | (1u << 7) | (1u << 10) | (16u << 17) |
-                        (static_cast<uint32_t>(rows_per_item >> 4) << 24);
+                        (static_cast<uint32_t>(dmt::kAttnM >> 4) << 24);
   ap.idesc_s = base;
   ap.idesc_o = base | (1u << 16);
   ap.O = static_cast<__nv_bfloat16*>(O);
