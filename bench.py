@@ -270,25 +270,19 @@ def time_device(p, A, B, C, steps, warmup, flush, stream, barrier):
 
 
 def time_e2e(p, steps, warmup, stream, dev):
-    """Metric through the C ABI with host buffers: per step H2D of A and B
-    from pinned memory, the call, D2H of C; CUDA events around all three."""
+    """The metric through the host-buffer C ABI (bmm_host_run), the call a
+    user with operands in host memory makes: per step A and B (and C_in when
+    beta != 0) go in from pinned host memory and C comes back, inside the
+    call, which overlaps those transfers with the computation in chunks.
+    CUDA events around the steps on the caller's stream."""
     import torch
     from dense_matmul_tensor_gb300 import bmm
     hA, hB, hC = host_inputs(p)
     hA, hB, hC = hA.pin_memory(), hB.pin_memory(), hC.pin_memory()
-    dA = torch.empty_like(hA, device=dev)
-    dB = torch.empty_like(hB, device=dev)
-    dC = torch.empty_like(hC, device=dev)
-    out = torch.empty_like(hC).pin_memory()
-    plan = bmm.Plan(desc_of(p))
+    plan = bmm.HostPlan(desc_of(p))
 
     def step():
-        dA.copy_(hA, non_blocking=True)
-        dB.copy_(hB, non_blocking=True)
-        if p.beta != 0.0:
-            dC.copy_(hC, non_blocking=True)
-        plan.run(dA, dB, dC, p.alpha, p.beta, stream)
-        out.copy_(dC, non_blocking=True)
+        plan.run(hA, hB, hC, p.alpha, p.beta, stream)
 
     with torch.cuda.stream(stream):
         for _ in range(warmup):
@@ -300,12 +294,16 @@ def time_e2e(p, steps, warmup, stream, dev):
             step()
         e1.record(stream)
     torch.cuda.synchronize()
+    st, word = plan.device_error()
+    chunks = plan.chunks()
     plan.close()
+    if st != bmm.BMM_OK:
+        raise RuntimeError(f"device error {word:#x} in the end-to-end leg")
     ms = e0.elapsed_time(e1) / steps
     h2d = hA.numel() * hA.element_size() + hB.numel() * hB.element_size() + \
         (hC.numel() * hC.element_size() if p.beta != 0.0 else 0)
     d2h = hC.numel() * hC.element_size()
-    return ms, h2d, d2h
+    return ms, h2d, d2h, chunks
 
 
 def grouped_measure(dev, stream, steps, count=1000, seed=7):
@@ -597,11 +595,12 @@ def main():
 
     if not args.no_e2e:
         e2e_steps = max(5, min(args.steps, 50))
-        ms_e, h2d, d2h = time_e2e(p, e2e_steps, 3, stream, dev)
+        ms_e, h2d, d2h, chunks = time_e2e(p, e2e_steps, 3, stream, dev)
         ms_e = max_over_ranks(ms_e)
         line["e2e"] = {"value": whole_job_tflops(p.flops(), world, ms_e), "unit": "TFLOP/s",
                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                       "ms_per_step": ms_e}
+                       "ms_per_step": ms_e, "api": "bmm_host_run",
+                       "chunks": chunks[0], "chunked_by": "rows" if chunks[1] else "batch items"}
 
     if not args.no_other:
         other = []

@@ -28,7 +28,9 @@ EXPORTED = ("bmm_create", "bmm_plan_query", "bmm_get_plan_info", "bmm_run",
             "bmm_get_device_error", "bmm_destroy", "bmm_status_string", "bmm_version",
             "bmm_grouped_create", "bmm_grouped_run", "bmm_grouped_get_device_error",
             "bmm_grouped_get_info", "bmm_grouped_destroy",
-            "bmm_attn_create", "bmm_attn_run", "bmm_attn_get_device_error", "bmm_attn_destroy")
+            "bmm_attn_create", "bmm_attn_run", "bmm_attn_get_device_error", "bmm_attn_destroy",
+            "bmm_host_create", "bmm_host_run", "bmm_host_get_device_error", "bmm_host_get_chunks",
+            "bmm_host_destroy")
 
 
 class bmm_desc_t(ctypes.Structure):
@@ -374,6 +376,72 @@ class AttnPlan:
     def close(self):
         if self.handle:
             bmm_attn_destroy(self.handle)
+            self.handle = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+# ------------------------------------------------------------ host buffers
+
+def _host_lib():
+    lib = load_library()
+    if lib.bmm_host_create.argtypes is None:
+        vp, P, i32 = ctypes.c_void_p, ctypes.POINTER, ctypes.c_int32
+        lib.bmm_host_create.argtypes = [P(bmm_desc_t), i32, P(vp)]
+        lib.bmm_host_create.restype = ctypes.c_int
+        lib.bmm_host_run.argtypes = [vp, vp, vp, vp, ctypes.c_float, ctypes.c_float, vp]
+        lib.bmm_host_run.restype = ctypes.c_int
+        lib.bmm_host_get_device_error.argtypes = [vp, P(ctypes.c_uint32)]
+        lib.bmm_host_get_device_error.restype = ctypes.c_int
+        lib.bmm_host_get_chunks.argtypes = [vp, P(i32), P(i32)]
+        lib.bmm_host_get_chunks.restype = ctypes.c_int
+        lib.bmm_host_destroy.argtypes = [vp]
+        lib.bmm_host_destroy.restype = ctypes.c_int
+    return lib
+
+
+class HostPlan:
+    """C = alpha op(A) op(B) + beta C from and to host memory, transfers
+    overlapped with the computation: ``with HostPlan(desc) as p: p.run(hA,
+    hB, hC, alpha, beta, stream)`` (hA, hB, hC: CPU tensors, ideally pinned)."""
+
+    def __init__(self, desc: bmm_desc_t, chunks: int = 0):
+        self.desc = desc
+        self.handle = ctypes.c_void_p()
+        st = _host_lib().bmm_host_create(ctypes.byref(desc), int(chunks), ctypes.byref(self.handle))
+        if st != BMM_OK:
+            self.handle = None
+            raise BmmError(st, "bmm_host_create")
+
+    def run(self, A, B, C, alpha=1.0, beta=0.0, stream=None):
+        st = _host_lib().bmm_host_run(self.handle, _ptr(A), _ptr(B), _ptr(C), float(alpha),
+                                      float(beta), _stream(stream))
+        if st != BMM_OK:
+            raise BmmError(st, "bmm_host_run")
+
+    def chunks(self):
+        c, r = ctypes.c_int32(), ctypes.c_int32()
+        _host_lib().bmm_host_get_chunks(self.handle, ctypes.byref(c), ctypes.byref(r))
+        return c.value, bool(r.value)
+
+    def device_error(self):
+        w = ctypes.c_uint32(0)
+        st = _host_lib().bmm_host_get_device_error(self.handle, ctypes.byref(w))
+        return st, w.value
+
+    def close(self):
+        if self.handle:
+            _host_lib().bmm_host_destroy(self.handle)
             self.handle = None
 
     def __enter__(self):

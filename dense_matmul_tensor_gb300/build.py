@@ -15,7 +15,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 LIBDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIBDIR, "libdmt_bmm.so")
-SOURCES = [os.path.join(CSRC, "bmm_api.cu"), os.path.join(CSRC, "attn_api.cu")]
+SOURCES = [os.path.join(CSRC, "bmm_api.cu"), os.path.join(CSRC, "attn_api.cu"),
+           os.path.join(CSRC, "host_api.cu")]
 DEPENDS = SOURCES + [os.path.join(CSRC, f) for f in ("bmm_kernel.cuh", "ptx.cuh", "attn_kernel.cuh")] + [
     os.path.join(ROOT, "include", "bmm.h")]
 OBJDIR = os.path.join(LIBDIR, "obj")

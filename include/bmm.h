@@ -261,6 +261,43 @@ BMM_API bmm_status_t bmm_attn_get_device_error(bmm_attn_plan_t plan, uint32_t* d
 BMM_API bmm_status_t bmm_attn_destroy(bmm_attn_plan_t plan);
 
 /*
+ * Host-buffer form: A, B (and C_in when beta != 0) are read from host memory,
+ * C is written back to host memory, in the layouts `desc` describes (the same
+ * strides as on the device).  The plan owns device copies of the operands and
+ * two copy streams; the work is cut into chunks of whole batch items (batch
+ * >= 2) or of 256-row blocks of A and C (batch 1, A row-major), and chunk c's
+ * inputs are copied in while chunk c-1 computes and chunk c-2's C is copied
+ * out.  The result is bit for bit the one bmm_run gives (the chunks split
+ * independent rows or batch items).  Host buffers should be page-locked
+ * (cudaHostAlloc / cudaHostRegister) for the copies to overlap; pageable
+ * memory works but serialises.  This is the call the end-to-end throughput
+ * is measured through.
+ */
+typedef struct bmm_host_plan_s* bmm_host_plan_t;
+
+/* Validate `desc` (as bmm_create), plan `chunks` pipeline chunks (0: four;
+ * at most 16; fewer when the problem has fewer batch items or 256-row
+ * blocks; one when batch is 1 and A is stored transposed), allocate the
+ * device copies, streams and events.  BMM_ERR_INVALID_ARG, BMM_ERR_UNSUPPORTED,
+ * BMM_ERR_NO_DEVICE or BMM_ERR_CUDA on failure (*plan set to NULL). */
+BMM_API bmm_status_t bmm_host_create(const bmm_desc_t* desc, int32_t chunks, bmm_host_plan_t* plan);
+
+/* C = alpha op(A) op(B) + beta C with host pointers A, B, C.  Asynchronous:
+ * ordered after the work already queued on `stream`, and `stream` completes
+ * once C is in host memory.  One run of a plan in flight at a time. */
+BMM_API bmm_status_t bmm_host_run(bmm_host_plan_t plan, const void* A, const void* B, void* C,
+                                  float alpha, float beta, void* stream);
+
+/* The first device error word among the chunks' plans (as bmm_get_device_error). */
+BMM_API bmm_status_t bmm_host_get_device_error(bmm_host_plan_t plan, uint32_t* detail);
+
+/* The chunk count and whether chunks are row blocks (1) or batch items (0). */
+BMM_API bmm_status_t bmm_host_get_chunks(bmm_host_plan_t plan, int32_t* chunks, int32_t* by_rows);
+
+/* Free the plan: its device copies, streams, events and the chunks' plans. */
+BMM_API bmm_status_t bmm_host_destroy(bmm_host_plan_t plan);
+
+/*
  * bmm_run without any allocation, for callers that cannot call cudaMalloc:
  * code running under an allocator that owns the device's memory (a caching
  * pool, a fixed budget reserved up front) and latency-critical call paths

@@ -215,3 +215,24 @@ def test_attention_create_without_a_gpu_reports_no_device(lib):
     with pytest.raises(api.BmmError) as e:
         api.bmm_attn_create(_attn())
     assert e.value.status == api.BMM_ERR_NO_DEVICE
+
+
+def test_host_plan_validates_before_any_device_call(lib):
+    import ctypes
+    lib = api._host_lib()  # argument types set
+    plan = ctypes.c_void_p(1)
+    assert lib.bmm_host_create(ctypes.byref(_desc(M=-1)), 0, ctypes.byref(plan)) == api.BMM_ERR_INVALID_ARG
+    assert plan.value is None
+    assert lib.bmm_host_create(ctypes.byref(_desc()), 17, ctypes.byref(plan)) == api.BMM_ERR_INVALID_ARG
+    assert lib.bmm_host_create(None, 0, ctypes.byref(plan)) == api.BMM_ERR_INVALID_ARG
+    assert lib.bmm_host_destroy(None) == api.BMM_OK
+    assert lib.bmm_host_run(None, None, None, None, 1.0, 0.0, None) == api.BMM_ERR_INVALID_ARG
+
+
+def test_host_plan_without_a_gpu_reports_no_device(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    with pytest.raises(api.BmmError) as e:
+        api.HostPlan(_desc())
+    assert e.value.status == api.BMM_ERR_NO_DEVICE
