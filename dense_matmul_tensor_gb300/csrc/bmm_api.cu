@@ -688,6 +688,8 @@ struct bmm_grouped_plan_s {
   int64_t smem_bytes, tiles;
   int sms;
   std::vector<dmt::GroupEntry> host;   // staging copy of the device table
+  std::vector<bmm_group_problem_t> last;  // pointers and scalars the device table holds
+  bool table_valid = false;               // the device table matches `host`
   dmt::GroupEntry* table;
   uint32_t* err;
   uint64_t timeout_ns;
@@ -740,7 +742,9 @@ bool prepare_grouped_kernel() {
 template <int BN>
 cudaError_t launch_grouped(const bmm_grouped_plan_s* pl, const KParams& kp, cudaStream_t stream) {
   if (!prepare_grouped_kernel<BN>()) return cudaErrorInvalidValue;
-  const int64_t grid = pl->tiles < pl->sms ? pl->tiles : pl->sms;
+  // one CTA per tile: running CTAs take the tiles of CTAs that have not
+  // started (cluster launch control), so the load balances itself
+  const int64_t grid = pl->tiles;
   CUtensorMap unused;
   std::memset(&unused, 0, sizeof(unused));
   dmt::bmm_tc_kernel<BN, true><<<static_cast<unsigned>(grid), dmt::kThreads,
@@ -833,6 +837,11 @@ bmm_status_t bmm_grouped_create(int32_t count, const bmm_group_problem_t* proble
     pl->live.push_back(i);
     pl->host.push_back(e);
   }
+  // one CTA per tile, and tile indices travel as int32 in the kernel's schedule
+  if (pl->tiles > 0x7fffffffLL) {
+    delete pl;
+    return BMM_ERR_UNSUPPORTED;
+  }
   const size_t table_bytes = sizeof(dmt::GroupEntry) * (pl->host.empty() ? 1 : pl->host.size());
   if (cudaMalloc(reinterpret_cast<void**>(&pl->table), table_bytes) != cudaSuccess) {
     delete pl;
@@ -856,6 +865,8 @@ bmm_status_t bmm_grouped_run(bmm_grouped_plan_t pl, const bmm_group_problem_t* p
   cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
   const int64_t ces = pl->typeC == BMM_F32 ? 4 : 2;
   const int b_box = pl->bn;
+  if (pl->last.size() != pl->live.size()) pl->last.assign(pl->live.size(), bmm_group_problem_t{});
+  bool changed = !pl->table_valid;
   for (size_t j = 0; j < pl->live.size(); ++j) {
     const int32_t i = pl->live[j];
     const bmm_group_problem_t& q = problems[i];
@@ -865,6 +876,16 @@ bmm_status_t bmm_grouped_run(bmm_grouped_plan_t pl, const bmm_group_problem_t* p
     if (!q.A || !q.B || !q.C) return BMM_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(q.A) & 15u) || (reinterpret_cast<uintptr_t>(q.B) & 15u))
       return BMM_ERR_MISALIGNED;
+    // an entry is re-encoded only when its operands or scalars moved
+    const bmm_group_problem_t& l = pl->last[j];
+    if (pl->table_valid && q.A == l.A && q.B == l.B && q.C == l.C && q.alpha == l.alpha &&
+        q.beta == l.beta)
+      continue;
+    // from here the device table no longer matches: an error return below
+    // leaves it marked stale, so the next run encodes every entry again
+    changed = true;
+    pl->table_valid = false;
+    pl->last[j] = q;
     dmt::GroupEntry& e = pl->host[j];
     const int64_t a_rows = pl->transA ? q.K : q.M, a_cols = pl->transA ? q.M : q.K;
     const int64_t b_rows = pl->transB ? q.N : q.K, b_cols = pl->transB ? q.K : q.N;
@@ -881,10 +902,13 @@ bmm_status_t bmm_grouped_run(bmm_grouped_plan_t pl, const bmm_group_problem_t* p
     e.beta = q.beta;
   }
   // Pageable source: the copy is staged before this call returns, so the host
-  // table may be rewritten by the next run.
-  if (cudaMemcpyAsync(pl->table, pl->host.data(), sizeof(dmt::GroupEntry) * pl->host.size(),
-                      cudaMemcpyHostToDevice, stream) != cudaSuccess)
-    return BMM_ERR_CUDA;
+  // table may be rewritten by the next run.  Skipped when no entry changed.
+  if (changed) {
+    if (cudaMemcpyAsync(pl->table, pl->host.data(), sizeof(dmt::GroupEntry) * pl->host.size(),
+                        cudaMemcpyHostToDevice, stream) != cudaSuccess)
+      return BMM_ERR_CUDA;
+    pl->table_valid = true;
+  }
 
   KParams kp;
   std::memset(&kp, 0, sizeof(kp));

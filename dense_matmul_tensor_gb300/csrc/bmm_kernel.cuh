@@ -65,6 +65,7 @@ enum WaitSite : uint32_t {
   kSiteMmaFull = 3,
   kSiteEpiAccFull = 4,
   kSiteTestStall = 5,
+  kSiteSchedule = 6,
 };
 
 // One problem of a grouped launch: an entry of a device table built by the
@@ -439,6 +440,14 @@ __device__ __forceinline__ void store_chunk_tma(const EpiArgs& p, const CUtensor
 // kGrouped: the launch covers a table of independent problems (p.groups):
 // every role maps its tile to a problem and takes that problem's sizes,
 // tensor maps and C from the table; otherwise one batched problem.
+// Tiles of a grouped launch differ in cost (K, and so the k-block count,
+// varies by problem), so they are handed out dynamically with cluster launch
+// control: the launch has one CTA per tile, each running CTA starts with its
+// own tile and then cancels CTAs that have not started yet and takes their
+// tiles.  The producer thread asks for the next tile while it loads the
+// current one and passes each tile index (or the end) to the MMA thread and
+// the epilogue warps through a four-entry ring in shared memory.  A plain
+// launch hands tiles out round-robin over a persistent grid.
 template <int BN, bool kGrouped = false>
 __global__ void __launch_bounds__(kThreads, 1)
     bmm_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUtensorMap tmA,
@@ -463,6 +472,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto accf_bar = [&](int a) { return bar0 + 8u * (2 * S + a); };
   auto acce_bar = [&](int a) { return bar0 + 8u * (2 * S + 2 + a); };
   const uint32_t drain_bar = bar0 + 8u * (2 * S + 4);
+  // dynamic schedule (grouped launches): the cancel response, the tile ring
+  // and its barriers, from byte 256 of the barrier block
+  const uint32_t clc_resp = bar0 + 256;
+  volatile int32_t* sched_tile = reinterpret_cast<volatile int32_t*>(smem + ring_bytes + kEpiBytes + 272u);
+  auto sched_full = [&](uint32_t i) { return bar0 + 288u + 8u * i; };
+  auto sched_empty = [&](uint32_t i) { return bar0 + 320u + 8u * i; };
+  const uint32_t clc_bar = bar0 + 352u;
+  constexpr uint32_t kSched = 4;
+  constexpr bool kDyn = kGrouped;  // grouped launches are scheduled dynamically
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -477,9 +495,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(acce_bar(a), 4);  // one arrive per epilogue warp
     }
     mbar_init(drain_bar, 1);
+    if constexpr (kDyn) {
+      for (uint32_t i = 0; i < kSched; ++i) {
+        mbar_init(sched_full(i), 1);
+        mbar_init(sched_empty(i), 5);  // the MMA thread and the four epilogue warps
+      }
+      mbar_init(clc_bar, 1);
+    }
     *abort_flag = 0u;
     fence_barrier_init();
   }
+
   if (warp == 0 && lane == 0 && !kGrouped) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
@@ -494,13 +520,48 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
   const Abort ab{abort_flag, p.err, p.timeout_ns};
+  // Tile i of this CTA for the MMA thread and the epilogue warps: round-robin
+  // over a persistent grid, or read from the schedule ring (lane 0 waits and
+  // releases the entry, the warp takes its value).  >= p.tiles: no more.
+  auto next_tile = [&](uint32_t i, int64_t& t) -> bool {
+    if constexpr (!kDyn) {
+      t = static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(i) * gridDim.x;
+      return true;
+    } else {
+      int v = 0, w = 1;
+      if (lane == 0) {
+        w = wait_bounded(sched_full(i % kSched), (i / kSched) & 1u, ab, kSiteSchedule) ? 1 : 0;
+        if (w) {
+          v = sched_tile[i % kSched];
+          mbar_arrive(sched_empty(i % kSched));
+        }
+      }
+      w = __shfl_sync(__activemask(), w, 0);
+      v = __shfl_sync(__activemask(), v, 0);
+      t = v;
+      return w != 0;
+    }
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer
     if (lane == 0) {
       uint32_t it = 0;
       bool ok = true;
-      for (int64_t t = blockIdx.x; t < p.tiles && ok; t += gridDim.x) {
+      int64_t t = blockIdx.x;
+      uint32_t si = 0;              // schedule entries published (grouped)
+      bool cancel_pending = false;  // a cancel request whose response has not been read
+      if constexpr (kDyn) {
+        sched_tile[0] = static_cast<int32_t>(t);
+        mbar_arrive(sched_full(0));
+        si = 1;
+      }
+      while (t < p.tiles && ok) {
+        if constexpr (kDyn) {  // ask for the next tile while this one loads
+          mbar_arrive_expect_tx(clc_bar, 16);
+          clc_try_cancel(clc_resp, clc_bar);
+          cancel_pending = true;
+        }
         const TileCtx tc = tile_ctx<kGrouped>(t, p, &tmA, &tmB, &tmC);
         const int m0 = tc.mb * kTileM, n0 = tc.nb * BN;
         const int za = p.a_bcast ? 0 : tc.b, zb = p.b_bcast ? 0 : tc.b;
@@ -528,6 +589,32 @@ __global__ void __launch_bounds__(kThreads, 1)
               tma_load_3d(b_dst + 8192u * h, tc.map_b, full_bar(s), n0 + 64 * h, k0, zb);
           }
         }
+        if constexpr (kDyn) {
+          // publish the next tile (a cancelled CTA's) or the end
+          int64_t nxt = p.tiles;
+          if (!ok || !wait_bounded<true>(clc_bar, (si - 1) & 1u, ab, kSiteSchedule)) {
+            ok = false;
+            break;
+          }
+          cancel_pending = false;
+          uint32_t x = 0;
+          if (clc_decode(clc_resp, x) && static_cast<int64_t>(x) < p.tiles) nxt = x;
+          const uint32_t slot = si % kSched;
+          if (si >= kSched &&
+              !wait_bounded<true>(sched_empty(slot), ((si / kSched) - 1u) & 1u, ab, kSiteSchedule)) {
+            ok = false;
+            break;
+          }
+          sched_tile[slot] = static_cast<int32_t>(nxt);
+          mbar_arrive(sched_full(slot));
+          ++si;
+          t = nxt;
+        } else {
+          t += gridDim.x;
+        }
+      }
+      if constexpr (kDyn) {  // a cancel response still on its way must land first
+        if (cancel_pending) drain_wait(clc_bar, (si - 1) & 1u);
       }
       // Let the loads issued for the last S k-blocks land before the CTA can
       // exit (after a normal run they have all landed and this returns at once).
@@ -547,7 +634,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Failure-detection test: phase 0 of the drain barrier completes only
       // after this thread's final commit, so this wait must run out.
       bool ok = !p.test_stall || wait_bounded(drain_bar, 0u, ab, kSiteTestStall);
-      for (int64_t t = blockIdx.x; t < p.tiles && ok; t += gridDim.x, ++tl) {
+      for (uint32_t ti = 0; ok; ++ti, ++tl) {
+        int64_t t;
+        if (!next_tile(ti, t)) {
+          ok = false;
+          break;
+        }
+        if (t >= p.tiles) break;
         const uint32_t acc = tl & 1u, aph = (tl >> 1) & 1u;
         if (!wait_bounded<true>(acce_bar(acc), aph ^ 1u, ab, kSiteMmaAccEmpty)) {
           ok = false;
@@ -595,7 +688,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t boxes_addr = smem_addr(boxes);
     uint32_t nbox = 0;
     uint32_t tl = 0;
-    for (int64_t t = blockIdx.x; t < p.tiles; t += gridDim.x, ++tl) {
+    for (uint32_t ti = 0;; ++ti, ++tl) {
+      int64_t t;
+      if (!next_tile(ti, t) || t >= p.tiles) break;
       const uint32_t acc = tl & 1u, aph = (tl >> 1) & 1u;
       const TileCtx tc = tile_ctx<kGrouped>(t, p, &tmA, &tmB, &tmC);
       const int b = tc.b, mb = tc.mb, nb = tc.nb;

@@ -173,6 +173,33 @@ __device__ __forceinline__ void tc_mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, 
       : "memory");
 }
 
+// Cluster launch control: ask to cancel a CTA (cluster) of this grid that has
+// not started yet; the 16-byte response lands in shared memory at `resp` and
+// completes 16 transaction bytes on `bar`.
+__device__ __forceinline__ void clc_try_cancel(uint32_t resp, uint32_t bar) {
+  asm volatile(
+      "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 [%0], [%1];"
+      ::"r"(resp), "r"(bar)
+      : "memory");
+}
+
+// Decode a cancel response: true and the cancelled CTA's x index when it
+// succeeded, false when no CTA was left to cancel.
+__device__ __forceinline__ bool clc_decode(uint32_t resp, uint32_t& ctaid_x) {
+  uint32_t ok, x = 0;
+  asm volatile(
+      "{\n\t.reg .b128 r;\n\t.reg .pred p;\n\t"
+      "ld.shared.b128 r, [%2];\n\t"
+      "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, r;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t"
+      "@p clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, r;\n\t}"
+      : "=r"(ok), "+r"(x)
+      : "r"(resp)
+      : "memory");
+  ctaid_x = x;
+  return ok != 0;
+}
+
 // Arrive once on `bar` when every tcgen05 op this thread issued so far is done.
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
   asm volatile(

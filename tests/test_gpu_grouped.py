@@ -140,3 +140,48 @@ def test_grouped_rejections():
         assert e.value.status == api.BMM_ERR_INVALID_ARG
     finally:
         api.bmm_grouped_destroy(plan)
+
+
+def test_reused_plan_follows_moved_outputs_and_new_scalars():
+    """A grouped plan caches each problem's tensor maps and table entry by its
+    pointers and scalars: run it, then with some problems writing to new C
+    buffers and a new alpha, then with the original arguments again; every
+    run must match the oracle (and the launch is dynamic: one CTA per tile,
+    cluster launch control handing tiles out)."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    dev = torch.device("cuda:0")
+    problems = _problems(24, 77, False, True, "bf16", "f32", with_beta=False)
+    xs = [wl.make_inputs(p) for p in problems]
+    keep, items = [], []
+    for p, x in zip(problems, xs):
+        s = p.strides()
+        A = torch.from_numpy(x.A.view(np.int16)).to(dev)
+        B = torch.from_numpy(x.B.view(np.int16)).to(dev)
+        C = torch.full((max(p.storage_elems()[2], 1),), float("nan"), device=dev)
+        keep += [A, B, C]
+        items.append(dict(M=p.M, N=p.N, K=p.K, lda=s["lda"], ldb=s["ldb"], ldc=s["ldc"], A=A, B=B, C=C,
+                          alpha=p.alpha, beta=0.0))
+    arr, n = api.make_problems(items)
+    plan = api.bmm_grouped_create(arr, n, 0, 1, "bf16", "f32")
+    try:
+        def run_and_check(its, alphas):
+            arr2, _ = api.make_problems(its)
+            api.bmm_grouped_run(plan, arr2, torch.cuda.current_stream())
+            torch.cuda.synchronize()
+            assert api.bmm_grouped_get_device_error(plan)[0] == api.BMM_OK
+            for p, x, it, a in zip(problems, xs, its, alphas):
+                q = wl.Problem(**{**p.__dict__, "alpha": a})
+                _check(q, x, it["C"].cpu().numpy())
+
+        run_and_check(items, [p.alpha for p in problems])
+        moved = [dict(it) for it in items]
+        for j in range(0, len(moved), 3):             # every third problem: new C, new alpha
+            moved[j]["C"] = torch.full_like(items[j]["C"], float("nan"))
+            moved[j]["alpha"] = 2.0
+        run_and_check(moved, [2.0 if j % 3 == 0 else p.alpha for j, p in enumerate(problems)])
+        for it in items:
+            it["C"].fill_(float("nan"))
+        run_and_check(items, [p.alpha for p in problems])
+    finally:
+        api.bmm_grouped_destroy(plan)
