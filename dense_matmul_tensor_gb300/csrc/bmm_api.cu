@@ -691,6 +691,7 @@ struct bmm_grouped_plan_s {
   std::vector<bmm_group_problem_t> last;  // pointers and scalars the device table holds
   bool table_valid = false;               // the device table matches `host`
   dmt::GroupEntry* table;
+  int32_t* first_tile;                    // device: each table entry's first tile (for the search)
   uint32_t* err;
   uint64_t timeout_ns;
 };
@@ -847,9 +848,24 @@ bmm_status_t bmm_grouped_create(int32_t count, const bmm_group_problem_t* proble
     delete pl;
     return BMM_ERR_CUDA;
   }
+  // the entries' first tiles as a compact int32 array: the kernel's
+  // tile -> problem search reads 4 bytes per entry (cache resident) instead
+  // of one 512-byte table record per step.  Fixed at create: sizes are.
+  std::vector<int32_t> first(pl->host.empty() ? 1 : pl->host.size(), 0);
+  for (size_t j = 0; j < pl->host.size(); ++j) first[j] = static_cast<int32_t>(pl->host[j].tile_begin);
+  pl->first_tile = nullptr;
+  if (cudaMalloc(reinterpret_cast<void**>(&pl->first_tile), first.size() * sizeof(int32_t)) != cudaSuccess ||
+      cudaMemcpy(pl->first_tile, first.data(), first.size() * sizeof(int32_t), cudaMemcpyHostToDevice) !=
+          cudaSuccess) {
+    cudaFree(pl->table);
+    cudaFree(pl->first_tile);
+    delete pl;
+    return BMM_ERR_CUDA;
+  }
   if (cudaMalloc(reinterpret_cast<void**>(&pl->err), 256) != cudaSuccess ||
       cudaMemset(pl->err, 0, 256) != cudaSuccess) {
     cudaFree(pl->table);
+    cudaFree(pl->first_tile);
     cudaFree(pl->err);
     delete pl;
     return BMM_ERR_CUDA;
@@ -925,6 +941,7 @@ bmm_status_t bmm_grouped_run(bmm_grouped_plan_t pl, const bmm_group_problem_t* p
   kp.err = pl->err;
   kp.timeout_ns = pl->timeout_ns;
   kp.groups = pl->table;
+  kp.group_first = pl->first_tile;
   kp.ngroups = static_cast<int32_t>(pl->host.size());
   cudaError_t e;
   switch (pl->bn) {
@@ -957,6 +974,7 @@ bmm_status_t bmm_grouped_destroy(bmm_grouped_plan_t pl) {
   if (!pl) return BMM_OK;
   bmm_status_t st = BMM_OK;
   if (pl->table && cudaFree(pl->table) != cudaSuccess) st = BMM_ERR_CUDA;
+  if (pl->first_tile && cudaFree(pl->first_tile) != cudaSuccess) st = BMM_ERR_CUDA;
   if (pl->err && cudaFree(pl->err) != cudaSuccess) st = BMM_ERR_CUDA;
   delete pl;
   return st;

@@ -105,6 +105,7 @@ struct KParams {
   uint64_t timeout_ns;     // bound on any single wait
   int32_t test_stall;      // 1: the MMA thread first waits on a barrier nothing completes
   const GroupEntry* groups;// grouped launches: the problem table (device memory)
+  const int32_t* group_first;  // ... and each entry's first tile, compact
   int32_t ngroups;
 };
 
@@ -233,6 +234,33 @@ struct TileCtx {
   const GroupEntry* g;
 };
 
+// Grouped launches: the table entry that tile t belongs to (the last whose
+// first tile is <= t), by binary search over the compact first-tile array.
+__device__ __forceinline__ int group_of(int64_t t, const KParams& p) {
+  int lo = 0, hi = p.ngroups - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(p.group_first + mid) <= t) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Tile context of tile t of table entry gi (grouped launches).
+__device__ __forceinline__ TileCtx tile_ctx_group(int64_t t, int gi, const KParams& p) {
+  TileCtx c;
+  const GroupEntry* g = p.groups + gi;
+  decode_mn(static_cast<int>(t - g->tile_begin), g->num_m, g->num_n, c.mb, c.nb);
+  c.b = 0;
+  c.k_blocks = g->k_blocks;
+  c.tail_steps = g->tail_steps;
+  c.map_a = &g->map_a;
+  c.map_b = &g->map_b;
+  c.map_c = &g->map_c;
+  c.g = g;
+  return c;
+}
+
 template <bool kGrouped>
 __device__ __forceinline__ TileCtx tile_ctx(int64_t t, const KParams& p, const CUtensorMap* tmA,
                                             const CUtensorMap* tmB, const CUtensorMap* tmC) {
@@ -246,21 +274,7 @@ __device__ __forceinline__ TileCtx tile_ctx(int64_t t, const KParams& p, const C
     c.map_c = tmC;
     c.g = nullptr;
   } else {
-    int lo = 0, hi = p.ngroups - 1;  // last problem whose first tile is <= t
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (p.groups[mid].tile_begin <= t) lo = mid;
-      else hi = mid - 1;
-    }
-    const GroupEntry* g = p.groups + lo;
-    decode_mn(static_cast<int>(t - g->tile_begin), g->num_m, g->num_n, c.mb, c.nb);
-    c.b = 0;
-    c.k_blocks = g->k_blocks;
-    c.tail_steps = g->tail_steps;
-    c.map_a = &g->map_a;
-    c.map_b = &g->map_b;
-    c.map_c = &g->map_c;
-    c.g = g;
+    c = tile_ctx_group(t, group_of(t, p), p);
   }
   return c;
 }
@@ -476,6 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // and its barriers, from byte 256 of the barrier block
   const uint32_t clc_resp = bar0 + 256;
   volatile int32_t* sched_tile = reinterpret_cast<volatile int32_t*>(smem + ring_bytes + kEpiBytes + 272u);
+  volatile int32_t* sched_group = reinterpret_cast<volatile int32_t*>(smem + ring_bytes + kEpiBytes + 368u);
   auto sched_full = [&](uint32_t i) { return bar0 + 288u + 8u * i; };
   auto sched_empty = [&](uint32_t i) { return bar0 + 320u + 8u * i; };
   const uint32_t clc_bar = bar0 + 352u;
@@ -521,26 +536,38 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
   const Abort ab{abort_flag, p.err, p.timeout_ns};
   // Tile i of this CTA for the MMA thread and the epilogue warps: round-robin
-  // over a persistent grid, or read from the schedule ring (lane 0 waits and
-  // releases the entry, the warp takes its value).  >= p.tiles: no more.
-  auto next_tile = [&](uint32_t i, int64_t& t) -> bool {
+  // over a persistent grid, or read from the schedule ring with its table
+  // entry (lane 0 waits and releases the entry, the lanes in `mask` take its
+  // values: all 32 for an epilogue warp, lane 0 alone for the MMA thread; a
+  // full-warp shuffle also gathers the warp back after lane 0's wait).
+  // >= p.tiles: no more.
+  auto next_tile = [&](uint32_t i, int64_t& t, int& gi, uint32_t mask) -> bool {
     if constexpr (!kDyn) {
       t = static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(i) * gridDim.x;
+      gi = 0;
       return true;
     } else {
-      int v = 0, w = 1;
+      int v = 0, gv = 0, w = 1;
       if (lane == 0) {
         w = wait_bounded(sched_full(i % kSched), (i / kSched) & 1u, ab, kSiteSchedule) ? 1 : 0;
         if (w) {
           v = sched_tile[i % kSched];
+          gv = sched_group[i % kSched];
           mbar_arrive(sched_empty(i % kSched));
         }
       }
-      w = __shfl_sync(__activemask(), w, 0);
-      v = __shfl_sync(__activemask(), v, 0);
+      w = __shfl_sync(mask, w, 0);
+      v = __shfl_sync(mask, v, 0);
+      gv = __shfl_sync(mask, gv, 0);
       t = v;
+      gi = gv;
       return w != 0;
     }
+  };
+  // the tile context from a tile and (dynamic schedule) its table entry
+  auto ctx_of = [&](int64_t t, int gi) -> TileCtx {
+    if constexpr (kDyn) return tile_ctx_group(t, gi, p);
+    else return tile_ctx<kGrouped>(t, p, &tmA, &tmB, &tmC);
   };
 
   if (warp == 0) {
@@ -551,8 +578,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       int64_t t = blockIdx.x;
       uint32_t si = 0;              // schedule entries published (grouped)
       bool cancel_pending = false;  // a cancel request whose response has not been read
+      int gi = 0;  // table entry of tile t (dynamic schedule)
       if constexpr (kDyn) {
+        gi = group_of(t, p);
         sched_tile[0] = static_cast<int32_t>(t);
+        sched_group[0] = gi;
         mbar_arrive(sched_full(0));
         si = 1;
       }
@@ -562,7 +592,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           clc_try_cancel(clc_resp, clc_bar);
           cancel_pending = true;
         }
-        const TileCtx tc = tile_ctx<kGrouped>(t, p, &tmA, &tmB, &tmC);
+        const TileCtx tc = ctx_of(t, gi);
         const int m0 = tc.mb * kTileM, n0 = tc.nb * BN;
         const int za = p.a_bcast ? 0 : tc.b, zb = p.b_bcast ? 0 : tc.b;
         for (int kb = 0; kb < tc.k_blocks; ++kb, ++it) {
@@ -605,10 +635,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
+          const int ngi = nxt < p.tiles ? group_of(nxt, p) : 0;
           sched_tile[slot] = static_cast<int32_t>(nxt);
+          sched_group[slot] = ngi;
           mbar_arrive(sched_full(slot));
           ++si;
           t = nxt;
+          gi = ngi;
         } else {
           t += gridDim.x;
         }
@@ -636,7 +669,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = !p.test_stall || wait_bounded(drain_bar, 0u, ab, kSiteTestStall);
       for (uint32_t ti = 0; ok; ++ti, ++tl) {
         int64_t t;
-        if (!next_tile(ti, t)) {
+        int gi;
+        if (!next_tile(ti, t, gi, 1u)) {  // lane 0 only
           ok = false;
           break;
         }
@@ -650,7 +684,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t d_tmem = tmem_base + acc * BN;
         int k_blocks = p.k_blocks, tail_steps = p.tail_steps;
         if constexpr (kGrouped) {
-          const TileCtx tc = tile_ctx<true>(t, p, &tmA, &tmB, &tmC);
+          const TileCtx tc = ctx_of(t, gi);
           k_blocks = tc.k_blocks;
           tail_steps = tc.tail_steps;
         }
@@ -690,9 +724,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t tl = 0;
     for (uint32_t ti = 0;; ++ti, ++tl) {
       int64_t t;
-      if (!next_tile(ti, t) || t >= p.tiles) break;
+      int gi;
+      if (!next_tile(ti, t, gi, 0xffffffffu) || t >= p.tiles) break;
       const uint32_t acc = tl & 1u, aph = (tl >> 1) & 1u;
-      const TileCtx tc = tile_ctx<kGrouped>(t, p, &tmA, &tmB, &tmC);
+      const TileCtx tc = ctx_of(t, gi);
       const int b = tc.b, mb = tc.mb, nb = tc.nb;
       EpiArgs ea = epi_args(p);
       if constexpr (kGrouped) {
