@@ -137,26 +137,18 @@ __device__ __forceinline__ float extreme32(const float (&v)[32], int valid, floa
   return kMin ? fminf(a, b) : fmaxf(a, b);
 }
 
-// Largest alpha * log2(e) * s over the valid keys of this thread's row of an
-// S block (128 columns at taddr); the first 64 scores stay in `v`.  kMin:
-// alpha < 0, so the smallest raw score gives the largest scaled one.
+// Loads this thread's row of an S block (128 columns at taddr) into `v` with
+// one wait, and returns the largest alpha * log2(e) * s over its valid keys.
+// kMin: alpha < 0, so the smallest raw score gives the largest scaled one.
 template <bool kMin>
 __device__ __forceinline__ float row_max_scaled(uint32_t taddr, int valid, float sc,
-                                                float (&v)[2][32]) {
-  float acc = kMin ? INFINITY : -INFINITY;
-  {  // the second half first: it is read again later
-    float u[2][32];
-    tmem_ld_32cols(taddr + 64u, u[0]);
-    tmem_ld_32cols(taddr + 96u, u[1]);
-    tmem_wait_ld();
-    acc = extreme32<kMin>(u[0], valid - 64, acc);
-    acc = extreme32<kMin>(u[1], valid - 96, acc);
-  }
-  tmem_ld_32cols(taddr, v[0]);
-  tmem_ld_32cols(taddr + 32u, v[1]);
+                                                float (&v)[4][32]) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) tmem_ld_32cols(taddr + 32u * c, v[c]);
   tmem_wait_ld();
-  acc = extreme32<kMin>(v[0], valid, acc);
-  acc = extreme32<kMin>(v[1], valid - 32, acc);
+  float acc = kMin ? INFINITY : -INFINITY;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) acc = extreme32<kMin>(v[c], valid - 32 * c, acc);
   return acc * sc;  // at least one key of the block is valid: finite
 }
 
@@ -386,7 +378,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const int valid = p.Lk - j * kAttnN < 128 ? p.Lk - j * kAttnN : 128;
         if (!(ok = warp_wait(s_full(x), n & 1u, ab, kSiteEpiAccFull, lane))) break;
         tc_fence_after_sync();
-        float v[2][32];
+        // this thread's whole 128-column row of S: one Tensor Memory round trip
+        float v[4][32];
         const float m_blk = sc >= 0.0f ? row_max_scaled<false>(s_col, valid, sc, v)
                                        : row_max_scaled<true>(s_col, valid, sc, v);
         const bool grow = j > 0 && m_blk > m + kAttnRescaleLog2;
@@ -410,24 +403,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           }
           tmem_wait_st();
         }
-        // P over the first 64 columns of S_X: keys 0..63 from registers,
-        // keys 64..127 read again (their S columns are not overwritten)
+        // P over the first 64 columns of S_X (keys 32c..32c+31 into columns
+        // 16c..16c+15): every score is already in registers
         const float nm = -m;
         float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f, s3 = 0.0f;
-        {
-          float w[32];
-          exp_pack(v[0], 0, valid, sc, nm, w, s0, s1, s2, s3);
-          exp_pack(v[1], 32, valid, sc, nm, w + 16, s0, s1, s2, s3);
-          tmem_ld_32cols(s_col + 64u, v[0]);
-          tmem_ld_32cols(s_col + 96u, v[1]);
-          tmem_wait_ld();
-          tmem_st_32cols(s_col, w);
-        }
-        {
-          float w[32];
-          exp_pack(v[0], 64, valid, sc, nm, w, s0, s1, s2, s3);
-          exp_pack(v[1], 96, valid, sc, nm, w + 16, s0, s1, s2, s3);
-          tmem_st_32cols(s_col + 32u, w);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          float w[16];
+          exp_pack(v[c], 32 * c, valid, sc, nm, w, s0, s1, s2, s3);
+          tmem_st_16cols(s_col + 16u * c, w);
         }
         // l sums the unrounded p: the bf16 rounding then perturbs only the
         // numerator of O = (P V) / l, by at most 2^-8 sum_c p_c |V_c| / l
