@@ -338,9 +338,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           // P_X(j) is warpgroup X's (ti * nb + j)-th block: every item has nb blocks
           const uint32_t pph = (ti * static_cast<uint32_t>(nb) + static_cast<uint32_t>(j)) & 1u;
           for (uint32_t x = 0; x < 2 && ok; ++x) {
-            if (!wait_bounded<true>(p_ready(x), pph, ab, kSiteMmaFull) ||
+            // V and O first, the softmax's release last: each wait costs the
+            // MMA thread a barrier round trip, and only the last one sits
+            // between the release and the next MMA
+            if ((x == 0 && !wait_bounded<true>(v_full(vs), vph, ab, kSiteMmaFull)) ||
                 (j == 0 && !wait_bounded<true>(o_empty(x), (ti & 1u) ^ 1u, ab, kSiteMmaAccEmpty)) ||
-                (x == 0 && !wait_bounded<true>(v_full(vs), vph, ab, kSiteMmaFull))) {
+                !wait_bounded<true>(p_ready(x), pph, ab, kSiteMmaFull)) {
               ok = false;
               break;
             }
