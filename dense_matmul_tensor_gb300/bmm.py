@@ -211,7 +211,8 @@ def bmm_run_noalloc(desc: bmm_desc_t, A, B, C, alpha=1.0, beta=0.0, stream=None,
     afford cudaMalloc's cost and device synchronisation).  Plans ``desc`` for
     this call and uses only the library's built-in device scratch (32 MiB of
     operand staging plus an error word, shared by all calls: serialise calls
-    whose GPU work would overlap).  ``device_error`` is an optional device
+    whose GPU work would overlap); operands that would need more staging are
+    read in place by the kernel's row loader.  ``device_error`` is an optional device
     pointer that receives the call's device error word on ``stream``."""
     lib = load_library()
     fn = lib.bmm_run_noalloc

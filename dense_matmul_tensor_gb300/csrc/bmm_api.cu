@@ -30,7 +30,8 @@ struct Operand {
   int64_t rows, cols;// stored matrix per batch item (row-major, `ld`)
   int64_t ld, stride;
   int bcast;         // one batch item shared by all
-  int pack;          // staged into the workspace first
+  int pack;          // 0: TMA from the caller's memory; 1: staged into the workspace
+                     // first; 2: read by the kernel's row loader (no staging)
   int64_t pld, pstride, ws_off;
   int box_rows;      // TMA box rows for a K-major operand (128 or BN)
 };
@@ -94,7 +95,14 @@ int balanced_tile_n(int64_t batch, int64_t Mv, int64_t Nv, int tile_m, int64_t u
 
 // Shape classes and resources.  Pure host arithmetic (no CUDA calls); `sms`
 // is the device's SM count (152 on GB300).
-void plan(const bmm_desc_t* d, Planned* P, int sms) {
+// row_loader: operands TMA cannot address go through the kernel's row loader
+// instead of the staging copy (DMT_BMM_LDG=1, or no workspace to stage in).
+bool row_loader_requested() {
+  const char* e = std::getenv("DMT_BMM_LDG");
+  return e && e[0] == '1';
+}
+
+void plan(const bmm_desc_t* d, Planned* P, int sms, bool row_loader) {
   std::memset(P, 0, sizeof(*P));
   // Skinny M: compute C^T = op(B)^T op(A)^T so that N fills the 128-row MMA.
   P->swap = (d->M <= 64 && d->N > d->M) ? 1 : 0;
@@ -172,8 +180,8 @@ void plan(const bmm_desc_t* d, Planned* P, int sms) {
     o->bcast = (o->stride == 0 || d->batch <= 1) ? 1 : 0;
     const bool ld_ok = (o->ld * 2) % 16 == 0;
     const bool st_ok = o->bcast || (o->stride * 2) % 16 == 0;
-    o->pack = (ld_ok && st_ok) ? 0 : 1;
-    if (o->pack) {
+    o->pack = (ld_ok && st_ok) ? 0 : (row_loader ? 2 : 1);
+    if (o->pack == 1) {
       o->pld = round_up(o->cols, 8);
       o->pstride = o->rows * o->pld;
       o->ws_off = ws;
@@ -186,7 +194,8 @@ void plan(const bmm_desc_t* d, Planned* P, int sms) {
   P->a_bytes = static_cast<uint32_t>(dmt::kTileM * dmt::kTileK * 2);
   const uint32_t b_bytes = static_cast<uint32_t>(b_rows * dmt::kTileK * 2);
   P->stage_bytes = static_cast<uint32_t>(round_up(P->a_bytes + b_bytes, 1024));
-  P->tx_bytes = P->a_bytes + b_bytes;
+  // TMA bytes per stage and CTA: the row loader's operands are not counted
+  P->tx_bytes = (P->a.pack == 2 ? 0u : P->a_bytes) + (P->b.pack == 2 ? 0u : b_bytes);
   const int64_t fixed = 1024 + dmt::kEpiBytes + dmt::kBarBytes;
   int stages = static_cast<int>((dmt::kSmemLimit - fixed) / P->stage_bytes);
   if (stages > 16) stages = 16;
@@ -404,7 +413,7 @@ bmm_status_t bmm_plan_query(const bmm_desc_t* desc, bmm_plan_info_t* info) {
   const bmm_status_t st = validate(desc);
   if (st != BMM_OK) return st;
   Planned P;
-  plan(desc, &P, kGb300Sms);
+  plan(desc, &P, kGb300Sms, row_loader_requested());
   fill_info(P, desc, info);
   (void)kGb300Sms;
   return BMM_OK;
@@ -429,7 +438,7 @@ bmm_status_t bmm_create(const bmm_desc_t* desc, bmm_plan_t* out) {
   bmm_plan_s* pl = new (std::nothrow) bmm_plan_s();
   if (!pl) return BMM_ERR_CUDA;
   pl->d = *desc;
-  plan(desc, &pl->P, sms);
+  plan(desc, &pl->P, sms, row_loader_requested());
   pl->device = dev;
   pl->sms = sms;
   pl->timeout_ns = wait_timeout_ns();
@@ -484,6 +493,11 @@ bmm_status_t bmm_run(bmm_plan_t pl, const void* A, const void* B, void* C, float
   for (int i = 0; i < 2; ++i) {
     const Operand& o = *ops[i];
     const void* src = o.user == 0 ? A : B;
+    if (o.pack == 2) {
+      if ((reinterpret_cast<uintptr_t>(src) & 1u) != 0) return BMM_ERR_MISALIGNED;
+      base[i] = src;  // read by the row loader: no tensor map
+      continue;
+    }
     if (o.pack) {
       uint16_t* dst = reinterpret_cast<uint16_t*>(static_cast<char*>(pl->ws) + o.ws_off);
       const int64_t nb = o.bcast ? 1 : d.batch;
@@ -525,6 +539,13 @@ bmm_status_t bmm_run(bmm_plan_t pl, const void* A, const void* B, void* C, float
   kp.tx_bytes = P.tx_bytes;
   kp.idesc = P.idesc;
   kp.tmem_cols = P.tmem_cols;
+  for (int i = 0; i < 2; ++i) {
+    const Operand& o = *ops[i];
+    if (o.pack != 2) continue;
+    kp.ldg_mask |= 1 << i;
+    kp.ldg[i] = dmt::LdgOperand{static_cast<const uint16_t*>(base[i]), o.ld, o.bcast ? 0 : o.stride,
+                                o.rows, o.cols};
+  }
   kp.C = C;
   kp.ldc = d.ldc;
   kp.sC = d.strideC;
@@ -649,8 +670,9 @@ extern "C" bmm_status_t bmm_run_noalloc(const bmm_desc_t* desc, const void* A, c
   bmm_plan_s pl;  // on the stack: nothing is allocated for the call
   std::memset(static_cast<void*>(&pl), 0, sizeof(pl));
   pl.d = *desc;
-  plan(desc, &pl.P, sms);
-  if (pl.P.workspace_bytes > static_cast<int64_t>(kNoAllocStagingMax)) return BMM_ERR_UNSUPPORTED;
+  plan(desc, &pl.P, sms, row_loader_requested());
+  // staging larger than the built-in scratch: the row loader reads those operands
+  if (pl.P.workspace_bytes > static_cast<int64_t>(kNoAllocStagingMax)) plan(desc, &pl.P, sms, true);
   unsigned char* scratch = nullptr;
   const bmm_status_t sst = noalloc_scratch(dev, &scratch);
   if (sst != BMM_OK) return sst;

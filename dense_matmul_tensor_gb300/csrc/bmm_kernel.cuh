@@ -1,7 +1,7 @@
 // The batched-product kernels for sm_103a.
 //
 // bmm_tc_kernel: a persistent, warp-specialised tcgen05 GEMM over the whole
-// batch x tile grid.  Per CTA (192 threads, one CTA per SM):
+// batch x tile grid.  Per CTA (256 threads, one CTA per SM):
 //   warp 0      TMA producer: fills a multi-stage shared-memory ring with the
 //               A tile (128 x 64) and the B tile (BN x 64) of each k-block.
 //   warp 1      allocates Tensor Memory and, from one lane, issues
@@ -12,6 +12,10 @@
 //               alpha (+ beta * C), convert, and store with coalesced
 //               global writes (row-major C goes through a padded shared
 //               staging tile so that each warp store covers one C row).
+//   warps 6..7  row loader, for an operand TMA cannot address (row or batch
+//               stride, or base, off a 16-byte boundary): plain loads of its
+//               elements, written into the stage in the layout the TMA box
+//               would give (idle otherwise).
 //
 // Design sources on the pages (prior art, restated for sm_103a):
 //  - "Triton Optimization Reference (cuTile -> Triton)", section 1: EVEN_K.
@@ -46,7 +50,8 @@ namespace dmt {
 constexpr int kTileM = 128;   // MMA M (TMEM lanes)
 constexpr int kTileK = 64;    // k-block: 64 x 16-bit = one 128-byte swizzle row
 constexpr int kUmmaK = 16;    // K of one tcgen05.mma kind::f16
-constexpr int kThreads = 192; // producer, MMA, 4 epilogue warps
+constexpr int kThreads = 256; // producer, MMA, 4 epilogue warps, 2 row-loader warps
+constexpr int kLdgWarps = 2;
 constexpr int kGroupM = 8;
 constexpr int kEpiPitch = 33; // floats per staged row (bank-conflict-free)
 // Epilogue staging, shared by the two store paths: four 32 x 33 fp32 tiles
@@ -81,6 +86,14 @@ struct alignas(128) GroupEntry {
   int32_t c_tma;
 };
 
+// An operand read by the row loader: [batch][rows][cols] 16-bit elements with
+// row stride ld and batch stride `stride` (0: one item for the whole batch).
+struct LdgOperand {
+  const uint16_t* ptr;
+  int64_t ld, stride;
+  int64_t rows, cols;
+};
+
 struct KParams {
   int32_t Mv, Nv, K;       // MMA view: D (Mv x Nv) = opA (Mv x K) * opB (K x Nv)
   int32_t num_m, num_n;    // tiles per batch item
@@ -107,6 +120,8 @@ struct KParams {
   const GroupEntry* groups;// grouped launches: the problem table (device memory)
   const int32_t* group_first;  // ... and each entry's first tile, compact
   int32_t ngroups;
+  int32_t ldg_mask;        // bit 0: A, bit 1: B read by the row loader (tx_bytes excludes them)
+  LdgOperand ldg[2];       // A, B
 };
 
 // What the epilogue needs about C, for the launch or for one grouped problem.
@@ -165,6 +180,79 @@ static __device__ __noinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   for (uint32_t it = 0; it < (1u << 24); ++it) {
     if (mbar_try_wait(bar, parity)) return;
     if ((it & 15u) == 0 && global_timer_ns() - t0 > 100000000ull) return;
+  }
+}
+
+template <bool B>
+struct BoolC {
+  static constexpr bool value = B;
+};
+
+// Bounded wait with cluster-scope acquire (see mbar_try_wait_spin_cluster).
+static __device__ __noinline__ bool wait_bounded_cluster(uint32_t bar, uint32_t parity, Abort ab, uint32_t site) {
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1; it < (1u << 30); ++it) {
+    if (mbar_try_wait_spin_cluster(bar, parity)) return true;
+    if ((it & 63u) == 0) {
+      if (*ab.flag) return false;
+      if (global_timer_ns() - t0 > ab.timeout_ns) break;
+    }
+  }
+  *ab.flag = 1u;
+  atomicCAS(ab.err, 0u, kErrTag | (site << 8) | (blockIdx.x & 0xFFu));
+  return false;
+}
+
+// Warp-uniform bounded wait (lane 0 polls, the warp takes its verdict).
+__device__ __forceinline__ bool warp_wait_bounded(uint32_t bar, uint32_t parity, Abort ab, uint32_t site,
+                                                  int lane) {
+  int w = 1;
+  if (lane == 0) w = wait_bounded<true>(bar, parity, ab, site) ? 1 : 0;
+  w = __shfl_sync(0xffffffffu, w, 0);
+  __syncwarp();
+  return w != 0;
+}
+
+// One operand tile of a ring stage written by the row loader, in the layout
+// a 128-byte-swizzled TMA box gives: rows of 64 contiguous elements (128
+// bytes), 16-byte chunk j of row r at chunk position j ^ (r mod 8); an
+// MN-major tile is `atoms` blocks of 64 such rows, 8 KB apart.  Storage row
+// row0 + r, elements col0 + 64 * atom + 8 * j .. + 7; elements outside the
+// operand are zero, as TMA fills them.  The chunks are spread over
+// `nthreads` threads (a multiple of 8; this thread is `tid`).
+__device__ __forceinline__ void ldg_fill(uint8_t* tile, const LdgOperand& o, int bz, int64_t row0,
+                                         int64_t col0, int tile_rows, int atoms, int tid, int nthreads) {
+  // thread tid takes chunk j = tid mod 8 of rows tid / 8, tid / 8 + nthreads / 8, ...
+  // (eight threads cover one 128-byte row), four rows' loads in flight together
+  constexpr int U = 4;
+  const int j = tid & 7, rstep = nthreads >> 3;
+  const uint16_t* base = o.ptr + static_cast<int64_t>(bz) * o.stride;
+  for (int a = 0; a < atoms; ++a) {
+    const int64_t scol = col0 + 64 * a + 8 * j;
+    const int64_t left = o.cols - scol;  // elements of this chunk inside the row
+    uint8_t* atom = tile + a * 8192;
+    for (int r0 = tid >> 3; r0 < tile_rows; r0 += U * rstep) {
+      uint32_t w[U][4];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int r = r0 + u * rstep;
+        const int64_t srow = row0 + r;
+        w[u][0] = w[u][1] = w[u][2] = w[u][3] = 0u;
+        if (r < tile_rows && srow < o.rows && left > 0) {
+          const uint16_t* s = base + srow * o.ld + scol;
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            if (e < left) w[u][e >> 1] |= static_cast<uint32_t>(__ldg(s + e)) << (16 * (e & 1));
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int r = r0 + u * rstep;
+        if (r < tile_rows)
+          *reinterpret_cast<uint4*>(atom + r * 128 + ((j ^ (r & 7)) << 4)) =
+              make_uint4(w[u][0], w[u][1], w[u][2], w[u][3]);
+      }
+    }
   }
 }
 
@@ -502,7 +590,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(full_bar(s), 1);
+      mbar_init(full_bar(s), 1 + (p.ldg_mask ? kLdgWarps : 0));  // + the row-loader warps
       mbar_init(empty_bar(s), 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -586,6 +674,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(sched_full(0));
         si = 1;
       }
+      // kLdg: some operand comes from the row loader (its TMA loads are
+      // skipped, and there may be no bytes to expect).  A separate copy of the
+      // loop keeps the TMA-only issue sequence as it is.
+      auto produce = [&](auto has_ldg) {
+      constexpr bool kLdg = decltype(has_ldg)::value;
       while (t < p.tiles && ok) {
         if constexpr (kDyn) {  // ask for the next tile while this one loads
           mbar_arrive_expect_tx(clc_bar, 16);
@@ -603,20 +696,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const uint32_t a_dst = sbase + s * p.stage_bytes;
           const uint32_t b_dst = a_dst + p.a_bytes;
-          mbar_arrive_expect_tx(full_bar(s), p.tx_bytes);
-          const int k0 = kb * kTileK;
-          if (!p.a_mn) {
-            tma_load_3d(a_dst, tc.map_a, full_bar(s), k0, m0, za);
+          if constexpr (kLdg) {
+            if (p.tx_bytes) mbar_arrive_expect_tx(full_bar(s), p.tx_bytes);
+            else mbar_arrive(full_bar(s));  // both operands come from the row loader
           } else {
-            tma_load_3d(a_dst, tc.map_a, full_bar(s), m0, k0, za);
-            tma_load_3d(a_dst + 8192u, tc.map_a, full_bar(s), m0 + 64, k0, za);
+            mbar_arrive_expect_tx(full_bar(s), p.tx_bytes);
           }
-          if (!p.b_mn) {
-            tma_load_3d(b_dst, tc.map_b, full_bar(s), k0, n0, zb);
-          } else {
+          const int k0 = kb * kTileK;
+          if (!kLdg || !(p.ldg_mask & 1)) {
+            if (!p.a_mn) {
+              tma_load_3d(a_dst, tc.map_a, full_bar(s), k0, m0, za);
+            } else {
+              tma_load_3d(a_dst, tc.map_a, full_bar(s), m0, k0, za);
+              tma_load_3d(a_dst + 8192u, tc.map_a, full_bar(s), m0 + 64, k0, za);
+            }
+          }
+          if (!kLdg || !(p.ldg_mask & 2)) {
+            if (!p.b_mn) {
+              tma_load_3d(b_dst, tc.map_b, full_bar(s), k0, n0, zb);
+            } else {
 #pragma unroll
-            for (int h = 0; h < BN / 64; ++h)
-              tma_load_3d(b_dst + 8192u * h, tc.map_b, full_bar(s), n0 + 64 * h, k0, zb);
+              for (int h = 0; h < BN / 64; ++h)
+                tma_load_3d(b_dst + 8192u * h, tc.map_b, full_bar(s), n0 + 64 * h, k0, zb);
+            }
           }
         }
         if constexpr (kDyn) {
@@ -646,6 +748,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           t += gridDim.x;
         }
       }
+      };
+      if (!kDyn && p.ldg_mask) produce(BoolC<true>{});
+      else produce(BoolC<false>{});
       if constexpr (kDyn) {  // a cancel response still on its way must land first
         if (cancel_pending) drain_wait(clc_bar, (si - 1) & 1u);
       }
@@ -714,7 +819,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_commit(drain_bar);
       drain_wait(drain_bar, 0u);
     }
-  } else {
+  } else if (warp < 6) {
     // --------------------------------------------------------- epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     float* stg = epi + (warp - 2) * 32 * kEpiPitch;
@@ -789,6 +894,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     if (lane == 0) bulk_wait_group_all();  // box stores done before shared memory is released
+  } else {
+    // ------------------------------------------------------- row loader
+    if constexpr (!kDyn) {
+      if (p.ldg_mask) {
+        const int tid = (warp - 6) * 32 + lane;
+        uint32_t it = 0;
+        bool ok = true;
+        for (int64_t t = blockIdx.x; t < p.tiles && ok; t += gridDim.x) {
+          int b, mb, nb;
+          decode_tile(t, p, b, mb, nb);
+          const int m0 = mb * kTileM, n0 = nb * BN;
+          for (int kb = 0; kb < p.k_blocks; ++kb, ++it) {
+            const uint32_t s = it % S, ph = (it / S) & 1u;
+            if (!(ok = warp_wait_bounded(empty_bar(s), ph ^ 1u, ab, kSiteProducerEmpty, lane))) break;
+            uint8_t* a_tile = smem + s * p.stage_bytes;
+            uint8_t* b_tile = a_tile + p.a_bytes;
+            const int k0 = kb * kTileK;
+            if (p.ldg_mask & 1)
+              ldg_fill(a_tile, p.ldg[0], p.a_bcast ? 0 : b, p.a_mn ? k0 : m0, p.a_mn ? m0 : k0,
+                       p.a_mn ? 64 : kTileM, p.a_mn ? 2 : 1, tid, kLdgWarps * 32);
+            if (p.ldg_mask & 2)
+              ldg_fill(b_tile, p.ldg[1], p.b_bcast ? 0 : b, p.b_mn ? k0 : n0, p.b_mn ? n0 : k0,
+                       p.b_mn ? 64 : BN, p.b_mn ? BN / 64 : 1, tid, kLdgWarps * 32);
+            fence_proxy_async_shared();  // the tensor core reads the stage through the async proxy
+            __syncwarp();
+            if (lane == 0) mbar_arrive(full_bar(s));
+          }
+        }
+      }
+    }
   }
 
   __syncwarp();
@@ -846,7 +981,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(full_bar(s), 1);
+      mbar_init(full_bar(s), 1 + (p.ldg_mask ? 2 * kLdgWarps : 0));  // + both CTAs' row loaders
       mbar_init(empty_bar(s), 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -878,6 +1013,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       uint32_t it = 0;
       bool ok = true;
+      // kLdg: some operand comes from the row loaders (its TMA loads are
+      // skipped, and the leader may have no bytes to expect).  A separate copy
+      // of the loop keeps the TMA-only issue sequence as it is.
+      auto produce = [&](auto has_ldg) {
+      constexpr bool kLdg = decltype(has_ldg)::value;
       for (int64_t t = pair; t < p.tiles && ok; t += npairs) {
         int b, mb, nb;
         decode_tile(t, p, b, mb, nb);
@@ -892,24 +1032,38 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const uint32_t a_dst = sbase + s * p.stage_bytes;
           const uint32_t b_dst = a_dst + p.a_bytes;
-          if (leader) mbar_arrive_expect_tx(full_bar(s), 2u * p.tx_bytes);
+          if constexpr (kLdg) {
+            if (leader) {
+              if (p.tx_bytes) mbar_arrive_expect_tx(full_bar(s), 2u * p.tx_bytes);
+              else mbar_arrive(full_bar(s));  // both operands come from the row loaders
+            }
+          } else {
+            if (leader) mbar_arrive_expect_tx(full_bar(s), 2u * p.tx_bytes);
+          }
           const uint32_t fb = mapa_shared(full_bar(s), 0);  // the leader's barrier
           const int k0 = kb * kTileK;
-          if (!p.a_mn) {
-            tma_load_3d_pair(a_dst, &tmA, fb, k0, m_own, za);
-          } else {
-            tma_load_3d_pair(a_dst, &tmA, fb, m_own, k0, za);
-            tma_load_3d_pair(a_dst + 8192u, &tmA, fb, m_own + 64, k0, za);
+          if (!kLdg || !(p.ldg_mask & 1)) {
+            if (!p.a_mn) {
+              tma_load_3d_pair(a_dst, &tmA, fb, k0, m_own, za);
+            } else {
+              tma_load_3d_pair(a_dst, &tmA, fb, m_own, k0, za);
+              tma_load_3d_pair(a_dst + 8192u, &tmA, fb, m_own + 64, k0, za);
+            }
           }
-          if (!p.b_mn) {
-            tma_load_3d_pair(b_dst, &tmB, fb, k0, n_own, zb);
-          } else {
+          if (!kLdg || !(p.ldg_mask & 2)) {
+            if (!p.b_mn) {
+              tma_load_3d_pair(b_dst, &tmB, fb, k0, n_own, zb);
+            } else {
 #pragma unroll
-            for (int h = 0; h < BNH / 64; ++h)
-              tma_load_3d_pair(b_dst + 8192u * h, &tmB, fb, n_own + 64 * h, k0, zb);
+              for (int h = 0; h < BNH / 64; ++h)
+                tma_load_3d_pair(b_dst + 8192u * h, &tmB, fb, n_own + 64 * h, k0, zb);
+            }
           }
         }
       }
+      };
+      if (p.ldg_mask) produce(BoolC<true>{});
+      else produce(BoolC<false>{});
       // The leader's full barriers count both CTAs' bytes: once the last S
       // have completed, no load of either CTA is still in flight.
       if (leader) {
@@ -927,6 +1081,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t sstep = p.stage_bytes >> 4;
       uint32_t s = 0, ph = 0, tl = 0;
       bool ok = !p.test_stall || wait_bounded(drain_bar, 0u, ab, kSiteTestStall);
+      // kClusterAcq: the peer's row loader writes its stage with plain stores,
+      // so the full waits take its release at cluster scope (a separate copy
+      // of the loop keeps the TMA-only path's issue loop as it is)
+      auto mma_tiles = [&](auto cluster_acq) {
+      constexpr bool kClusterAcq = decltype(cluster_acq)::value;
       for (int64_t t = pair; t < p.tiles && ok; t += npairs, ++tl) {
         const uint32_t acc = tl & 1u, aph = (tl >> 1) & 1u;
         if (!wait_bounded<true>(acce_bar(acc), aph ^ 1u, ab, kSiteMmaAccEmpty)) {
@@ -936,7 +1095,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + acc * BN;
         for (int kb = 0; kb < p.k_blocks; ++kb) {
-          if (!wait_bounded<true>(full_bar(s), ph, ab, kSiteMmaFull)) {
+          if (!(kClusterAcq ? wait_bounded_cluster(full_bar(s), ph, ab, kSiteMmaFull)
+                            : wait_bounded<true>(full_bar(s), ph, ab, kSiteMmaFull))) {
             ok = false;
             break;
           }
@@ -953,10 +1113,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         tc_commit_pair_multicast(accf_bar(acc), 0x3);  // accumulator halves complete
       }
+      };
+      if (p.ldg_mask) mma_tiles(BoolC<true>{});
+      else mma_tiles(BoolC<false>{});
       tc_commit_pair(drain_bar);
       drain_wait(drain_bar, 0u);
     }
-  } else {
+  } else if (warp < 6) {
     // ------------------------------------------------ epilogue (each CTA)
     const int q = warp & 3;
     float* stg = epi + (warp - 2) * 32 * kEpiPitch;
@@ -1013,6 +1176,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     if (lane == 0) bulk_wait_group_all();
+  } else {
+    // ---------------------------------------------- row loader (each CTA)
+    if (p.ldg_mask) {
+      const int tid = (warp - 6) * 32 + lane;
+      uint32_t it = 0;
+      bool ok = true;
+      for (int64_t t = pair; t < p.tiles && ok; t += npairs) {
+        int b, mb, nb;
+        decode_tile(t, p, b, mb, nb);
+        const int m_own = mb * (2 * kTileM) + static_cast<int>(rank) * kTileM;
+        const int n_own = nb * BN + static_cast<int>(rank) * BNH;
+        for (int kb = 0; kb < p.k_blocks; ++kb, ++it) {
+          const uint32_t s = it % S, ph = (it / S) & 1u;
+          if (!(ok = warp_wait_bounded(empty_bar(s), ph ^ 1u, ab, kSiteProducerEmpty, lane))) break;
+          uint8_t* a_tile = smem + s * p.stage_bytes;
+          uint8_t* b_tile = a_tile + p.a_bytes;
+          const int k0 = kb * kTileK;
+          if (p.ldg_mask & 1)
+            ldg_fill(a_tile, p.ldg[0], p.a_bcast ? 0 : b, p.a_mn ? k0 : m_own, p.a_mn ? m_own : k0,
+                     p.a_mn ? 64 : kTileM, p.a_mn ? 2 : 1, tid, kLdgWarps * 32);
+          if (p.ldg_mask & 2)
+            ldg_fill(b_tile, p.ldg[1], p.b_bcast ? 0 : b, p.b_mn ? k0 : n_own, p.b_mn ? n_own : k0,
+                     p.b_mn ? 64 : BNH, p.b_mn ? BNH / 64 : 1, tid, kLdgWarps * 32);
+          fence_proxy_async_shared();  // the tensor core reads the stage through the async proxy
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(mapa_shared(full_bar(s), 0));  // the leader's barrier
+        }
+      }
+    }
   }
 
   __syncwarp();

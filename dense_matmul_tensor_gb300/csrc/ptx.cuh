@@ -72,6 +72,21 @@ __device__ __forceinline__ bool mbar_try_wait_spin(uint32_t bar, uint32_t parity
   return ok != 0;
 }
 
+// As mbar_try_wait_spin, with acquire at cluster scope: orders this thread's
+// later accesses after writes that other CTAs of the cluster released to the
+// barrier (arrivals from a peer CTA's threads).
+__device__ __forceinline__ bool mbar_try_wait_spin_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, 0;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // ------------------------------------------------------------------ TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {

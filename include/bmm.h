@@ -94,7 +94,9 @@ typedef struct {
   int32_t tile_m, tile_n, tile_k; /* MMA-view tile (after any operand swap) */
   int32_t stages;                 /* shared-memory ring depth */
   int32_t swap_ab;                /* 1: computes C^T = op(B)^T op(A)^T (skinny M) */
-  int32_t pack_a, pack_b;         /* 1: operand staged through the workspace */
+  int32_t pack_a, pack_b;         /* 0: read in place by TMA; 1: staged through the
+                                     workspace first; 2: read in place by the
+                                     kernel's row loader (plain loads, no staging) */
   int32_t even_k;                 /* 1: K is a multiple of tile_k (no tail tile) */
   int32_t tmem_cols;              /* Tensor Memory columns allocated per CTA */
   int32_t cta_pair;               /* 1: tiles run on CTA pairs (2-SM MMA, tile_m = 256) */
@@ -141,8 +143,11 @@ BMM_API bmm_status_t bmm_get_plan_info(bmm_plan_t plan, bmm_plan_info_t* info);
  * is the legacy default stream).  A, B, C are device pointers owned by the
  * caller and laid out as `desc` said at bmm_create.  Operands that the plan
  * reads in place by TMA must have 16-byte-aligned base pointers; otherwise
- * BMM_ERR_MISALIGNED is returned and nothing is enqueued.  C needs only
- * element alignment.  Returns BMM_OK once the work is enqueued,
+ * BMM_ERR_MISALIGNED is returned and nothing is enqueued.  Operands whose row
+ * or batch strides are not 16-byte multiples are staged through the plan's
+ * workspace (or, with the environment variable DMT_BMM_LDG=1 at plan time,
+ * read in place by the kernel's row loader) and need only element
+ * alignment, as does C.  Returns BMM_OK once the work is enqueued,
  * BMM_ERR_INVALID_ARG (null plan or pointer), or BMM_ERR_CUDA (launch
  * failure).  Does not synchronise.
  */
@@ -308,10 +313,10 @@ BMM_API bmm_status_t bmm_host_destroy(bmm_host_plan_t plan);
  * bmm_run on `stream`.  Its only scratch is one device array inside the
  * library (every GPU that loads the library holds it until exit): a 256-byte
  * error-word region plus a 32 MiB staging area for operands whose strides or
- * batch strides are not multiples of 16 bytes.  A problem that would need
- * more staging than 32 MiB is rejected with BMM_ERR_UNSUPPORTED before
- * anything is enqueued.  It calls no cudaMalloc, cudaFree or allocating
- * library routine.
+ * batch strides are not multiples of 16 bytes.  When such operands would need
+ * more than 32 MiB of staging, the kernel's row loader reads them in place
+ * instead (slower per byte than TMA, but with no staging copy).  It calls no
+ * cudaMalloc, cudaFree or allocating library routine.
  *
  * The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call
