@@ -325,11 +325,16 @@ bool encode_map(const bmm_plan_s* pl, const Operand& o, const void* base, CUtens
   return r == CUDA_SUCCESS;
 }
 
+// Threads per CTA: the row-loader warps (6 and 7) only when an operand needs them.
+unsigned block_threads(const KParams& kp) {
+  return static_cast<unsigned>(kp.ldg_mask ? dmt::kThreads : dmt::kThreads - 32 * dmt::kLdgWarps);
+}
+
 cudaLaunchConfig_t pair_config(int64_t pairs, int64_t smem, cudaStream_t stream,
-                               cudaLaunchAttribute* attr) {
+                               cudaLaunchAttribute* attr, unsigned threads) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs), 1, 1);
-  cfg.blockDim = dim3(dmt::kThreads, 1, 1);
+  cfg.blockDim = dim3(threads, 1, 1);
   cfg.dynamicSmemBytes = static_cast<size_t>(smem);
   cfg.stream = stream;
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -348,14 +353,14 @@ cudaError_t launch_gemm_pair(bmm_plan_s* pl, const KParams& kp, cudaStream_t str
   if (!prepare_pair_kernel<BN>()) return cudaErrorInvalidValue;
   cudaLaunchAttribute attr[1];
   if (pl->max_pairs == 0) {
-    cudaLaunchConfig_t q = pair_config(pl->sms / 2, pl->P.smem_bytes, stream, attr);
+    cudaLaunchConfig_t q = pair_config(pl->sms / 2, pl->P.smem_bytes, stream, attr, dmt::kThreads);
     int n = 0;
     const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, dmt::bmm_tc2_kernel<BN>, &q);
     if (e != cudaSuccess) return e;
     pl->max_pairs = n > 0 ? n : 1;
   }
   const int64_t pairs = pl->P.tiles < pl->max_pairs ? pl->P.tiles : pl->max_pairs;
-  cudaLaunchConfig_t cfg = pair_config(pairs, pl->P.smem_bytes, stream, attr);
+  cudaLaunchConfig_t cfg = pair_config(pairs, pl->P.smem_bytes, stream, attr, block_threads(kp));
   return cudaLaunchKernelEx(&cfg, dmt::bmm_tc2_kernel<BN>, kp, pl->map[0], pl->map[1], pl->map[2]);
 }
 
@@ -383,7 +388,7 @@ template <int BN>
 cudaError_t launch_gemm(const bmm_plan_s* pl, const KParams& kp, cudaStream_t stream) {
   if (!prepare_kernel<BN>(pl->P.smem_bytes)) return cudaErrorInvalidValue;
   int64_t grid = pl->P.tiles < pl->sms ? pl->P.tiles : pl->sms;
-  dmt::bmm_tc_kernel<BN><<<static_cast<unsigned>(grid), dmt::kThreads,
+  dmt::bmm_tc_kernel<BN><<<static_cast<unsigned>(grid), block_threads(kp),
                            static_cast<size_t>(pl->P.smem_bytes), stream>>>(kp, pl->map[0],
                                                                            pl->map[1], pl->map[2]);
   return cudaGetLastError();
@@ -770,7 +775,7 @@ cudaError_t launch_grouped(const bmm_grouped_plan_s* pl, const KParams& kp, cuda
   const int64_t grid = pl->tiles;
   CUtensorMap unused;
   std::memset(&unused, 0, sizeof(unused));
-  dmt::bmm_tc_kernel<BN, true><<<static_cast<unsigned>(grid), dmt::kThreads,
+  dmt::bmm_tc_kernel<BN, true><<<static_cast<unsigned>(grid), block_threads(kp),
                                  static_cast<size_t>(pl->smem_bytes), stream>>>(kp, unused, unused, unused);
   return cudaGetLastError();
 }
