@@ -340,10 +340,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           for (uint32_t x = 0; x < 2 && ok; ++x) {
             // V and O first, the softmax's release last: each wait costs the
             // MMA thread a barrier round trip, and only the last one sits
-            // between the release and the next MMA
+            // between the release and the next MMA.  The release is awaited
+            // asleep (a suspend-time hint): the barrier's completion wakes the
+            // thread sooner than its next poll would see it.
             if ((x == 0 && !wait_bounded<true>(v_full(vs), vph, ab, kSiteMmaFull)) ||
                 (j == 0 && !wait_bounded<true>(o_empty(x), (ti & 1u) ^ 1u, ab, kSiteMmaAccEmpty)) ||
-                !wait_bounded<true>(p_ready(x), pph, ab, kSiteMmaFull)) {
+                !(mbar_try_wait_hint(p_ready(x), pph, 500u) ||
+                  wait_bounded<true>(p_ready(x), pph, ab, kSiteMmaFull))) {
               ok = false;
               break;
             }

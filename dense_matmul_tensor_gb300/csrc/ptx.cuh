@@ -87,6 +87,21 @@ __device__ __forceinline__ bool mbar_try_wait_spin_cluster(uint32_t bar, uint32_
   return ok != 0;
 }
 
+// Test with a suspend-time hint (ns): if the phase is not complete the thread
+// may sleep until it completes or the hint passes, and it is woken by the
+// completion itself rather than by its next poll.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // ------------------------------------------------------------------ TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
