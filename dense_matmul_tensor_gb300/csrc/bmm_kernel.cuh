@@ -678,76 +678,76 @@ __global__ void __launch_bounds__(kThreads, 1)
       // skipped, and there may be no bytes to expect).  A separate copy of the
       // loop keeps the TMA-only issue sequence as it is.
       auto produce = [&](auto has_ldg) {
-      constexpr bool kLdg = decltype(has_ldg)::value;
-      while (t < p.tiles && ok) {
-        if constexpr (kDyn) {  // ask for the next tile while this one loads
-          mbar_arrive_expect_tx(clc_bar, 16);
-          clc_try_cancel(clc_resp, clc_bar);
-          cancel_pending = true;
-        }
-        const TileCtx tc = ctx_of(t, gi);
-        const int m0 = tc.mb * kTileM, n0 = tc.nb * BN;
-        const int za = p.a_bcast ? 0 : tc.b, zb = p.b_bcast ? 0 : tc.b;
-        for (int kb = 0; kb < tc.k_blocks; ++kb, ++it) {
-          const uint32_t s = it % S, ph = (it / S) & 1u;
-          if (!wait_bounded<true>(empty_bar(s), ph ^ 1u, ab, kSiteProducerEmpty)) {
-            ok = false;
-            break;
+        constexpr bool kLdg = decltype(has_ldg)::value;
+        while (t < p.tiles && ok) {
+          if constexpr (kDyn) {  // ask for the next tile while this one loads
+            mbar_arrive_expect_tx(clc_bar, 16);
+            clc_try_cancel(clc_resp, clc_bar);
+            cancel_pending = true;
           }
-          const uint32_t a_dst = sbase + s * p.stage_bytes;
-          const uint32_t b_dst = a_dst + p.a_bytes;
-          if constexpr (kLdg) {
-            if (p.tx_bytes) mbar_arrive_expect_tx(full_bar(s), p.tx_bytes);
-            else mbar_arrive(full_bar(s));  // both operands come from the row loader
-          } else {
-            mbar_arrive_expect_tx(full_bar(s), p.tx_bytes);
-          }
-          const int k0 = kb * kTileK;
-          if (!kLdg || !(p.ldg_mask & 1)) {
-            if (!p.a_mn) {
-              tma_load_3d(a_dst, tc.map_a, full_bar(s), k0, m0, za);
-            } else {
-              tma_load_3d(a_dst, tc.map_a, full_bar(s), m0, k0, za);
-              tma_load_3d(a_dst + 8192u, tc.map_a, full_bar(s), m0 + 64, k0, za);
+          const TileCtx tc = ctx_of(t, gi);
+          const int m0 = tc.mb * kTileM, n0 = tc.nb * BN;
+          const int za = p.a_bcast ? 0 : tc.b, zb = p.b_bcast ? 0 : tc.b;
+          for (int kb = 0; kb < tc.k_blocks; ++kb, ++it) {
+            const uint32_t s = it % S, ph = (it / S) & 1u;
+            if (!wait_bounded<true>(empty_bar(s), ph ^ 1u, ab, kSiteProducerEmpty)) {
+              ok = false;
+              break;
             }
-          }
-          if (!kLdg || !(p.ldg_mask & 2)) {
-            if (!p.b_mn) {
-              tma_load_3d(b_dst, tc.map_b, full_bar(s), k0, n0, zb);
+            const uint32_t a_dst = sbase + s * p.stage_bytes;
+            const uint32_t b_dst = a_dst + p.a_bytes;
+            if constexpr (kLdg) {
+              if (p.tx_bytes) mbar_arrive_expect_tx(full_bar(s), p.tx_bytes);
+              else mbar_arrive(full_bar(s));  // both operands come from the row loader
             } else {
+              mbar_arrive_expect_tx(full_bar(s), p.tx_bytes);
+            }
+            const int k0 = kb * kTileK;
+            if (!kLdg || !(p.ldg_mask & 1)) {
+              if (!p.a_mn) {
+                tma_load_3d(a_dst, tc.map_a, full_bar(s), k0, m0, za);
+              } else {
+                tma_load_3d(a_dst, tc.map_a, full_bar(s), m0, k0, za);
+                tma_load_3d(a_dst + 8192u, tc.map_a, full_bar(s), m0 + 64, k0, za);
+              }
+            }
+            if (!kLdg || !(p.ldg_mask & 2)) {
+              if (!p.b_mn) {
+                tma_load_3d(b_dst, tc.map_b, full_bar(s), k0, n0, zb);
+              } else {
 #pragma unroll
-              for (int h = 0; h < BN / 64; ++h)
-                tma_load_3d(b_dst + 8192u * h, tc.map_b, full_bar(s), n0 + 64 * h, k0, zb);
+                for (int h = 0; h < BN / 64; ++h)
+                  tma_load_3d(b_dst + 8192u * h, tc.map_b, full_bar(s), n0 + 64 * h, k0, zb);
+              }
             }
           }
-        }
-        if constexpr (kDyn) {
-          // publish the next tile (a cancelled CTA's) or the end
-          int64_t nxt = p.tiles;
-          if (!ok || !wait_bounded<true>(clc_bar, (si - 1) & 1u, ab, kSiteSchedule)) {
-            ok = false;
-            break;
+          if constexpr (kDyn) {
+            // publish the next tile (a cancelled CTA's) or the end
+            int64_t nxt = p.tiles;
+            if (!ok || !wait_bounded<true>(clc_bar, (si - 1) & 1u, ab, kSiteSchedule)) {
+              ok = false;
+              break;
+            }
+            cancel_pending = false;
+            uint32_t x = 0;
+            if (clc_decode(clc_resp, x) && static_cast<int64_t>(x) < p.tiles) nxt = x;
+            const uint32_t slot = si % kSched;
+            if (si >= kSched &&
+                !wait_bounded<true>(sched_empty(slot), ((si / kSched) - 1u) & 1u, ab, kSiteSchedule)) {
+              ok = false;
+              break;
+            }
+            const int ngi = nxt < p.tiles ? group_of(nxt, p) : 0;
+            sched_tile[slot] = static_cast<int32_t>(nxt);
+            sched_group[slot] = ngi;
+            mbar_arrive(sched_full(slot));
+            ++si;
+            t = nxt;
+            gi = ngi;
+          } else {
+            t += gridDim.x;
           }
-          cancel_pending = false;
-          uint32_t x = 0;
-          if (clc_decode(clc_resp, x) && static_cast<int64_t>(x) < p.tiles) nxt = x;
-          const uint32_t slot = si % kSched;
-          if (si >= kSched &&
-              !wait_bounded<true>(sched_empty(slot), ((si / kSched) - 1u) & 1u, ab, kSiteSchedule)) {
-            ok = false;
-            break;
-          }
-          const int ngi = nxt < p.tiles ? group_of(nxt, p) : 0;
-          sched_tile[slot] = static_cast<int32_t>(nxt);
-          sched_group[slot] = ngi;
-          mbar_arrive(sched_full(slot));
-          ++si;
-          t = nxt;
-          gi = ngi;
-        } else {
-          t += gridDim.x;
         }
-      }
       };
       if (!kDyn && p.ldg_mask) produce(BoolC<true>{});
       else produce(BoolC<false>{});
@@ -1017,50 +1017,50 @@ __global__ void __launch_bounds__(kThreads, 1)
       // skipped, and the leader may have no bytes to expect).  A separate copy
       // of the loop keeps the TMA-only issue sequence as it is.
       auto produce = [&](auto has_ldg) {
-      constexpr bool kLdg = decltype(has_ldg)::value;
-      for (int64_t t = pair; t < p.tiles && ok; t += npairs) {
-        int b, mb, nb;
-        decode_tile(t, p, b, mb, nb);
-        const int m_own = mb * (2 * kTileM) + static_cast<int>(rank) * kTileM;
-        const int n_own = nb * BN + static_cast<int>(rank) * BNH;
-        const int za = p.a_bcast ? 0 : b, zb = p.b_bcast ? 0 : b;
-        for (int kb = 0; kb < p.k_blocks; ++kb, ++it) {
-          const uint32_t s = it % S, ph = (it / S) & 1u;
-          if (!wait_bounded<true>(empty_bar(s), ph ^ 1u, ab, kSiteProducerEmpty)) {
-            ok = false;
-            break;
-          }
-          const uint32_t a_dst = sbase + s * p.stage_bytes;
-          const uint32_t b_dst = a_dst + p.a_bytes;
-          if constexpr (kLdg) {
-            if (leader) {
-              if (p.tx_bytes) mbar_arrive_expect_tx(full_bar(s), 2u * p.tx_bytes);
-              else mbar_arrive(full_bar(s));  // both operands come from the row loaders
+        constexpr bool kLdg = decltype(has_ldg)::value;
+        for (int64_t t = pair; t < p.tiles && ok; t += npairs) {
+          int b, mb, nb;
+          decode_tile(t, p, b, mb, nb);
+          const int m_own = mb * (2 * kTileM) + static_cast<int>(rank) * kTileM;
+          const int n_own = nb * BN + static_cast<int>(rank) * BNH;
+          const int za = p.a_bcast ? 0 : b, zb = p.b_bcast ? 0 : b;
+          for (int kb = 0; kb < p.k_blocks; ++kb, ++it) {
+            const uint32_t s = it % S, ph = (it / S) & 1u;
+            if (!wait_bounded<true>(empty_bar(s), ph ^ 1u, ab, kSiteProducerEmpty)) {
+              ok = false;
+              break;
             }
-          } else {
-            if (leader) mbar_arrive_expect_tx(full_bar(s), 2u * p.tx_bytes);
-          }
-          const uint32_t fb = mapa_shared(full_bar(s), 0);  // the leader's barrier
-          const int k0 = kb * kTileK;
-          if (!kLdg || !(p.ldg_mask & 1)) {
-            if (!p.a_mn) {
-              tma_load_3d_pair(a_dst, &tmA, fb, k0, m_own, za);
+            const uint32_t a_dst = sbase + s * p.stage_bytes;
+            const uint32_t b_dst = a_dst + p.a_bytes;
+            if constexpr (kLdg) {
+              if (leader) {
+                if (p.tx_bytes) mbar_arrive_expect_tx(full_bar(s), 2u * p.tx_bytes);
+                else mbar_arrive(full_bar(s));  // both operands come from the row loaders
+              }
             } else {
-              tma_load_3d_pair(a_dst, &tmA, fb, m_own, k0, za);
-              tma_load_3d_pair(a_dst + 8192u, &tmA, fb, m_own + 64, k0, za);
+              if (leader) mbar_arrive_expect_tx(full_bar(s), 2u * p.tx_bytes);
             }
-          }
-          if (!kLdg || !(p.ldg_mask & 2)) {
-            if (!p.b_mn) {
-              tma_load_3d_pair(b_dst, &tmB, fb, k0, n_own, zb);
-            } else {
+            const uint32_t fb = mapa_shared(full_bar(s), 0);  // the leader's barrier
+            const int k0 = kb * kTileK;
+            if (!kLdg || !(p.ldg_mask & 1)) {
+              if (!p.a_mn) {
+                tma_load_3d_pair(a_dst, &tmA, fb, k0, m_own, za);
+              } else {
+                tma_load_3d_pair(a_dst, &tmA, fb, m_own, k0, za);
+                tma_load_3d_pair(a_dst + 8192u, &tmA, fb, m_own + 64, k0, za);
+              }
+            }
+            if (!kLdg || !(p.ldg_mask & 2)) {
+              if (!p.b_mn) {
+                tma_load_3d_pair(b_dst, &tmB, fb, k0, n_own, zb);
+              } else {
 #pragma unroll
-              for (int h = 0; h < BNH / 64; ++h)
-                tma_load_3d_pair(b_dst + 8192u * h, &tmB, fb, n_own + 64 * h, k0, zb);
+                for (int h = 0; h < BNH / 64; ++h)
+                  tma_load_3d_pair(b_dst + 8192u * h, &tmB, fb, n_own + 64 * h, k0, zb);
+              }
             }
           }
         }
-      }
       };
       if (p.ldg_mask) produce(BoolC<true>{});
       else produce(BoolC<false>{});
@@ -1085,34 +1085,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       // so the full waits take its release at cluster scope (a separate copy
       // of the loop keeps the TMA-only path's issue loop as it is)
       auto mma_tiles = [&](auto cluster_acq) {
-      constexpr bool kClusterAcq = decltype(cluster_acq)::value;
-      for (int64_t t = pair; t < p.tiles && ok; t += npairs, ++tl) {
-        const uint32_t acc = tl & 1u, aph = (tl >> 1) & 1u;
-        if (!wait_bounded<true>(acce_bar(acc), aph ^ 1u, ab, kSiteMmaAccEmpty)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after_sync();
-        const uint32_t d_tmem = tmem_base + acc * BN;
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
-          if (!(kClusterAcq ? wait_bounded_cluster(full_bar(s), ph, ab, kSiteMmaFull)
-                            : wait_bounded<true>(full_bar(s), ph, ab, kSiteMmaFull))) {
+        constexpr bool kClusterAcq = decltype(cluster_acq)::value;
+        for (int64_t t = pair; t < p.tiles && ok; t += npairs, ++tl) {
+          const uint32_t acc = tl & 1u, aph = (tl >> 1) & 1u;
+          if (!wait_bounded<true>(acce_bar(acc), aph ^ 1u, ab, kSiteMmaAccEmpty)) {
             ok = false;
             break;
           }
-          // No tcgen05 fence here (see the single-CTA kernel).
-          const int nsteps = (kb == p.k_blocks - 1) ? p.tail_steps : kTileK / kUmmaK;
-          issue_kblock<true>(d_tmem, alo0 + s * sstep, blo0 + s * sstep, hi, hi, astep, bstep,
-                             p.idesc, nsteps, kb == 0);
-          tc_commit_pair_multicast(empty_bar(s), 0x3);  // slot free in both CTAs
-          if (++s == static_cast<uint32_t>(S)) {
-            s = 0;
-            ph ^= 1u;
+          tc_fence_after_sync();
+          const uint32_t d_tmem = tmem_base + acc * BN;
+          for (int kb = 0; kb < p.k_blocks; ++kb) {
+            if (!(kClusterAcq ? wait_bounded_cluster(full_bar(s), ph, ab, kSiteMmaFull)
+                              : wait_bounded<true>(full_bar(s), ph, ab, kSiteMmaFull))) {
+              ok = false;
+              break;
+            }
+            // No tcgen05 fence here (see the single-CTA kernel).
+            const int nsteps = (kb == p.k_blocks - 1) ? p.tail_steps : kTileK / kUmmaK;
+            issue_kblock<true>(d_tmem, alo0 + s * sstep, blo0 + s * sstep, hi, hi, astep, bstep,
+                               p.idesc, nsteps, kb == 0);
+            tc_commit_pair_multicast(empty_bar(s), 0x3);  // slot free in both CTAs
+            if (++s == static_cast<uint32_t>(S)) {
+              s = 0;
+              ph ^= 1u;
+            }
           }
+          if (!ok) break;
+          tc_commit_pair_multicast(accf_bar(acc), 0x3);  // accumulator halves complete
         }
-        if (!ok) break;
-        tc_commit_pair_multicast(accf_bar(acc), 0x3);  // accumulator halves complete
-      }
       };
       if (p.ldg_mask) mma_tiles(BoolC<true>{});
       else mma_tiles(BoolC<false>{});
