@@ -213,18 +213,46 @@ __device__ __forceinline__ bool warp_wait_bounded(uint32_t bar, uint32_t parity,
   return w != 0;
 }
 
+// 16 bytes starting at even byte offset sh (0..14) of the 32 bytes lo:hi.
+__device__ __forceinline__ uint4 extract16(const uint4& lo, const uint4& hi, uint32_t sh) {
+  const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+  const uint32_t b = (sh & 3u) * 8u;  // bits: 0 or 16
+  uint32_t o[4];
+  switch (sh >> 2) {  // whole words: the same for every chunk of a row
+    case 0:
+#pragma unroll
+      for (int i = 0; i < 4; ++i) o[i] = __funnelshift_r(w[i], w[i + 1], b);
+      break;
+    case 1:
+#pragma unroll
+      for (int i = 0; i < 4; ++i) o[i] = __funnelshift_r(w[i + 1], w[i + 2], b);
+      break;
+    case 2:
+#pragma unroll
+      for (int i = 0; i < 4; ++i) o[i] = __funnelshift_r(w[i + 2], w[i + 3], b);
+      break;
+    default:
+#pragma unroll
+      for (int i = 0; i < 4; ++i) o[i] = __funnelshift_r(w[i + 3], w[i + 4], b);
+      break;
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 // One operand tile of a ring stage written by the row loader, in the layout
 // a 128-byte-swizzled TMA box gives: rows of 64 contiguous elements (128
 // bytes), 16-byte chunk j of row r at chunk position j ^ (r mod 8); an
 // MN-major tile is `atoms` blocks of 64 such rows, 8 KB apart.  Storage row
 // row0 + r, elements col0 + 64 * atom + 8 * j .. + 7; elements outside the
 // operand are zero, as TMA fills them.  The chunks are spread over
-// `nthreads` threads (a multiple of 8; this thread is `tid`).
+// `nthreads` threads (a multiple of 8; this thread is `tid`: chunk j =
+// tid mod 8 of every (nthreads / 8)-th row).  A chunk starts on any 2-byte
+// boundary: the thread loads the one or two 16-byte-aligned chunks that hold
+// it (a second one only if it holds bytes of the row) and shifts the 16 bytes
+// out; eight chunks' loads are in flight before the first store.
 __device__ __forceinline__ void ldg_fill(uint8_t* tile, const LdgOperand& o, int bz, int64_t row0,
                                          int64_t col0, int tile_rows, int atoms, int tid, int nthreads) {
-  // thread tid takes chunk j = tid mod 8 of rows tid / 8, tid / 8 + nthreads / 8, ...
-  // (eight threads cover one 128-byte row), four rows' loads in flight together
-  constexpr int U = 4;
+  constexpr int U = 8;
   const int j = tid & 7, rstep = nthreads >> 3;
   const uint16_t* base = o.ptr + static_cast<int64_t>(bz) * o.stride;
   for (int a = 0; a < atoms; ++a) {
@@ -232,25 +260,36 @@ __device__ __forceinline__ void ldg_fill(uint8_t* tile, const LdgOperand& o, int
     const int64_t left = o.cols - scol;  // elements of this chunk inside the row
     uint8_t* atom = tile + a * 8192;
     for (int r0 = tid >> 3; r0 < tile_rows; r0 += U * rstep) {
-      uint32_t w[U][4];
+      uint4 lo[U], hi[U];
+      uint32_t sh[U];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int r = r0 + u * rstep;
         const int64_t srow = row0 + r;
-        w[u][0] = w[u][1] = w[u][2] = w[u][3] = 0u;
+        lo[u] = hi[u] = make_uint4(0u, 0u, 0u, 0u);
+        sh[u] = 0u;
         if (r < tile_rows && srow < o.rows && left > 0) {
-          const uint16_t* s = base + srow * o.ld + scol;
-#pragma unroll
-          for (int e = 0; e < 8; ++e)
-            if (e < left) w[u][e >> 1] |= static_cast<uint32_t>(__ldg(s + e)) << (16 * (e & 1));
+          const uintptr_t at = reinterpret_cast<uintptr_t>(base + srow * o.ld + scol);
+          const uintptr_t q = at & ~static_cast<uintptr_t>(15);
+          const uintptr_t end = at + 2u * static_cast<uintptr_t>(left < 8 ? left : 8);
+          sh[u] = static_cast<uint32_t>(at - q);
+          lo[u] = __ldg(reinterpret_cast<const uint4*>(q));
+          if (q + 16u < end) hi[u] = __ldg(reinterpret_cast<const uint4*>(q) + 1);
         }
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int r = r0 + u * rstep;
-        if (r < tile_rows)
-          *reinterpret_cast<uint4*>(atom + r * 128 + ((j ^ (r & 7)) << 4)) =
-              make_uint4(w[u][0], w[u][1], w[u][2], w[u][3]);
+        if (r >= tile_rows) continue;
+        uint4 v = extract16(lo[u], hi[u], sh[u]);
+        if (left < 8) {  // zero the elements past the row end
+          uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            if (e >= left) w[e >> 1] &= (e & 1) ? 0x0000FFFFu : 0xFFFF0000u;
+          v = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        *reinterpret_cast<uint4*>(atom + r * 128 + ((j ^ (r & 7)) << 4)) = v;
       }
     }
   }
