@@ -16,7 +16,9 @@ measured dense bf16 peak; ``e2e`` repeats the metric with host buffers (H2D of
 A and B from pinned memory, the call, D2H of C inside each timed step);
 ``cpu_baseline`` times the fp64 oracle on the host cores on a bounded sample
 of the same workload.  ``other_workloads`` reports the remaining specified
-shapes (ragged, attention pair, skinny, small) measured the same way.
+shapes (ragged, attention pair, skinny, small) measured the same way; a shape
+with a staged operand also reports ``row_loader``, the same product with the
+kernels' row loader reading that operand in place.
 
 With ``--impl reference`` the reference arm runs instead: the fp64 CPU
 oracle, timed on this host's cores on a bounded sample of each step.
@@ -617,13 +619,23 @@ def main():
             mqm = statistics.fmean(mq)
             gbs = q.algorithmic_bytes() / (mqm * 1e-3) / 1e9
             tf = q.flops() / (mqm * 1e-3) / 1e12
-            other.append({"workload": name, "ms": mqm, "TFLOP/s": tf,
-                          "frac_bf16_peak": tf / peaks["bf16_tflops"], "GB/s": gbs,
-                          "frac_hbm": gbs / peaks["hbm_gbs"],
-                          "intensity_flop_per_byte": q.flops() / q.algorithmic_bytes(),
-                          "tile_n": qinfo.tile_n, "swap_ab": qinfo.swap_ab,
-                          "cta_pair": qinfo.cta_pair,
-                          "pack": [qinfo.pack_a, qinfo.pack_b]})
+            entry = {"workload": name, "ms": mqm, "TFLOP/s": tf,
+                     "frac_bf16_peak": tf / peaks["bf16_tflops"], "GB/s": gbs,
+                     "frac_hbm": gbs / peaks["hbm_gbs"],
+                     "intensity_flop_per_byte": q.flops() / q.algorithmic_bytes(),
+                     "tile_n": qinfo.tile_n, "swap_ab": qinfo.swap_ab,
+                     "cta_pair": qinfo.cta_pair,
+                     "pack": [qinfo.pack_a, qinfo.pack_b]}
+            if qinfo.pack_a == 1 or qinfo.pack_b == 1:
+                # the same product with the kernels' row loader instead of the
+                # staging copy (pack 2: read in place, no workspace)
+                os.environ["DMT_BMM_LDG"] = "1"
+                try:
+                    ml, linfo, _, _ = time_device(q, qa, qb, qc, qs, 3, flush, stream, lambda: None)
+                finally:
+                    del os.environ["DMT_BMM_LDG"]
+                entry["row_loader"] = {"ms": statistics.fmean(ml), "pack": [linfo.pack_a, linfo.pack_b]}
+            other.append(entry)
             del qa, qb, qc
             torch.cuda.empty_cache()
         line["other_workloads"] = other
