@@ -24,14 +24,18 @@
 //               P_X V_j reads P_X from Tensor Memory and V MN-major from
 //               shared memory.  While one warpgroup works on its scores the
 //               tensor core works on the other tile.
-//   warps 2..9  softmax: warpgroup X (warps 2..5: A, 6..9: B), one query row
-//               per thread.  It reads its row of S_X, takes the row maximum,
-//               writes p = exp2(s*alpha*log2e - m) as bf16 pairs over the
-//               first 64 columns of S_X (P_X), and at the end of the item
-//               stores its 128 rows of O_X / l.
+//   warps 2..9  softmax, all eight warps on tile A, then on tile B, per key
+//               block.  Warps w and w+4 share a Tensor Memory lane quarter and
+//               split each of its 32 rows: w takes keys 0..63 of the block,
+//               w+4 keys 64..127.  Each thread reads its 64 scores of S_X,
+//               trades its half-row maximum with its partner (a 64-thread
+//               named barrier), writes p = exp2(s*alpha*log2e - m) as bf16
+//               pairs into columns 32..95 of S_X (P_X; every thread writes
+//               only columns it has read), and at the end of the item stores
+//               its 64 columns of O_X / l.
 // Tensor Memory: S_A, S_B, O_A, O_B, 128 columns each.  The commit that
 // signals S_X(j) also covers P_X(j-1) V_{j-1} (a commit tracks every MMA
-// issued before it), so when a warpgroup sees its scores, O_X is final for
+// issued before it), so when the softmax warps see S_X, O_X is final for
 // the previous block and the columns it overwrites with P are free.
 //
 // Lazy rescale: m is the largest scaled score seen when O_X was last
@@ -55,9 +59,11 @@ constexpr uint32_t kAttnHalf = 128u * 128u;       // one 64-column half of 128 r
 constexpr uint32_t kAttnTile = 2u * kAttnHalf;    // Q, K or V tile: 32 KB
 constexpr uint32_t kAttnBarBytes = 256;
 // Q_A, Q_B, K[2], V[2]
-constexpr uint32_t kAttnSmem = 1024 + 6 * kAttnTile + kAttnBarBytes;
+constexpr uint32_t kAttnXchBytes = 2 * 2 * 128 * 8;  // two buffers x two key halves x 128 rows x (value, verdict)
+constexpr uint32_t kAttnSmem = 1024 + 6 * kAttnTile + kAttnBarBytes + kAttnXchBytes;
 static_assert(kAttnSmem <= 232448, "shared memory per CTA");
 constexpr float kAttnRescaleLog2 = 8.0f;  // lazy-rescale threshold
+constexpr uint32_t kAttnPCol = 32;        // P_X's first column within S_X
 
 struct AttnParams {
   int32_t Lq, Lk;
@@ -137,19 +143,26 @@ __device__ __forceinline__ float extreme32(const float (&v)[32], int valid, floa
   return kMin ? fminf(a, b) : fmaxf(a, b);
 }
 
-// Loads this thread's row of an S block (128 columns at taddr) into `v` with
-// one wait, and returns the largest alpha * log2(e) * s over its valid keys.
-// kMin: alpha < 0, so the smallest raw score gives the largest scaled one.
+// Loads this thread's half row of an S block (64 columns at taddr) into `v`
+// with one wait, and returns the largest alpha * log2(e) * s over its valid
+// keys (-inf when the half holds none).  kMin: alpha < 0, so the smallest raw
+// score gives the largest scaled one.
 template <bool kMin>
-__device__ __forceinline__ float row_max_scaled(uint32_t taddr, int valid, float sc,
-                                                float (&v)[4][32]) {
-#pragma unroll
-  for (int c = 0; c < 4; ++c) tmem_ld_32cols(taddr + 32u * c, v[c]);
+__device__ __forceinline__ float half_row_max_scaled(uint32_t taddr, int valid, float sc,
+                                                     float (&v)[2][32]) {
+  tmem_ld_32cols(taddr, v[0]);
+  tmem_ld_32cols(taddr + 32u, v[1]);
   tmem_wait_ld();
+  if (valid <= 0) return -INFINITY;
   float acc = kMin ? INFINITY : -INFINITY;
-#pragma unroll
-  for (int c = 0; c < 4; ++c) acc = extreme32<kMin>(v[c], valid - 32 * c, acc);
-  return acc * sc;  // at least one key of the block is valid: finite
+  acc = extreme32<kMin>(v[0], valid, acc);
+  acc = extreme32<kMin>(v[1], valid - 32, acc);
+  return acc * sc;
+}
+
+// Named barrier `id` over `count` threads (whole warps).
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 // p = exp2(s * sc - m) for 32 keys of the row (key0 = their first index
@@ -206,7 +219,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   auto o_full = [&](uint32_t x) { return bar0 + 112 + 8 * x; };  // the item's last P_X V done
   auto o_empty = [&](uint32_t x) { return bar0 + 128 + 8 * x; }; // O_X read out
   const uint32_t drain_bar = bar0 + 144;
-  constexpr uint32_t kGroupWarps = 4;
+  constexpr uint32_t kSoftmaxWarps = 8;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -219,9 +232,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       mbar_init(v_full(s), 1);
       mbar_init(v_empty(s), 1);
       mbar_init(s_full(s), 1);
-      mbar_init(p_ready(s), kGroupWarps);
+      mbar_init(p_ready(s), kSoftmaxWarps);
       mbar_init(o_full(s), 1);
-      mbar_init(o_empty(s), kGroupWarps);
+      mbar_init(o_empty(s), kSoftmaxWarps);
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0u;
@@ -318,12 +331,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
         return true;
       };
-      // O_X (+)= P_X V: P from the first 64 columns of S_X (8 per k-step), V
+      // O_X (+)= P_X V: P from columns 32..95 of S_X (8 per k-step), V
       // MN-major (64-column halves 16 KB apart, 16 keys = 2048 bytes per k-step)
       auto issue_pv = [&](uint32_t x, uint32_t vs, bool first) {
         const uint32_t v_lo = desc_lo(v_addr + vs * kAttnTile, kAttnHalf);
         const uint32_t d_tmem = tmem_base + 256u + x * 128u;
-        const uint32_t a_tmem = tmem_base + x * 128u;
+        const uint32_t a_tmem = tmem_base + x * 128u + kAttnPCol;
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
           tc_mma_f16_ts(d_tmem, a_tmem + 8u * ks, desc_join(v_lo + ks * 128u, hi_sw), p.idesc_o,
@@ -367,93 +380,142 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
   } else {
     // --------------------------------------------------------- softmax
-    const uint32_t x = static_cast<uint32_t>(warp - 2) >> 2;  // tile A (0) or B (1)
-    const int quad = warp & 3;                    // TMEM lane quarter this warp may access
-    const int row = quad * 32 + lane;             // query row within the tile
+    // Warps w and w + 4 may access the same Tensor Memory lane quarter: both
+    // take its 32 query rows in both tiles (A, then B, per key block), w the
+    // keys 0..63 of each block and w + 4 the keys 64..127.
+    const int quad = warp & 3;
+    const uint32_t h = static_cast<uint32_t>(warp - 2) >> 2;  // key half
+    const int row = quad * 32 + lane;                         // query row within a tile
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-    const uint32_t s_col = tmem_base + lane_off + x * 128u;          // S_X, and P_X over it
-    const uint32_t o_col = tmem_base + lane_off + 256u + x * 128u;   // O_X
     const float sc = p.scale_log2;
+    float2* xch = reinterpret_cast<float2*>(smem + 6 * kAttnTile + kAttnBarBytes);
+    uint32_t nx = 0;
+    // Trades a value and the wait verdict with the thread of the same row in
+    // the partner warp.  Two buffers: a thread rewrites a buffer only after
+    // the next barrier, which its partner passes only once it has read it.
+    // Both warps take every exchange, so a failed wait in either ends both
+    // loops at the same point.
+    auto exchange = [&](float mine, bool& ok_io) -> float {
+      float2* buf = xch + (nx++ & 1u) * 256u;
+      buf[h * 128u + row] = make_float2(mine, ok_io ? 1.0f : 0.0f);
+      named_bar_sync(1u + static_cast<uint32_t>(quad), 64u);
+      const float2 o = buf[(h ^ 1u) * 128u + row];
+      ok_io = ok_io && o.y != 0.0f;
+      return o.x;
+    };
     uint32_t n = 0, ti = 0;  // blocks done, items
     bool ok = true;
     for (int64_t item = blockIdx.x; item < p.items && ok; item += gridDim.x, ++ti) {
       const int b = static_cast<int>(item / p.q_tiles);
-      const int qi = static_cast<int>(item % p.q_tiles) * kAttnItemRows + static_cast<int>(x) * kAttnM + row;
-      float m = -INFINITY, l = 0.0f;
-      for (int j = 0; j < nb; ++j, ++n) {
+      // per tile: running maximum and this half's sum of p (kept in registers:
+      // the tile loop below is not unrolled, so no arrays indexed by it)
+      float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.0f, l_b = 0.0f;
+      for (int j = 0; j < nb && ok; ++j, ++n) {
         const int valid = p.Lk - j * kAttnN < 128 ? p.Lk - j * kAttnN : 128;
-        if (!(ok = warp_wait(s_full(x), n & 1u, ab, kSiteEpiAccFull, lane))) break;
-        tc_fence_after_sync();
-        // this thread's whole 128-column row of S: one Tensor Memory round trip
-        float v[4][32];
-        const float m_blk = sc >= 0.0f ? row_max_scaled<false>(s_col, valid, sc, v)
-                                       : row_max_scaled<true>(s_col, valid, sc, v);
-        const bool grow = j > 0 && m_blk > m + kAttnRescaleLog2;
-        if (j == 0) m = m_blk;
-        if (__any_sync(0xffffffffu, grow)) {
-          // rescale O_X and l by exp2(m_old - m_new) in the rows that need it
-          // (O_X is final for the previous block: see the header)
-          const float r = grow ? fast_exp2(m - m_blk) : 1.0f;
-          if (grow) {
-            l *= r;
-            m = m_blk;
-          }
+        const int valid_h = valid - 64 * static_cast<int>(h);  // keys of this half in range
 #pragma unroll 1
-          for (int c = 0; c < 8; ++c) {
-            float o[16];
-            tmem_ld_16cols(o_col + 16u * c, o);
-            tmem_wait_ld();
+        for (uint32_t x = 0; x < 2; ++x) {
+          const uint32_t s_col = tmem_base + lane_off + x * 128u;          // S_X
+          const uint32_t o_col = tmem_base + lane_off + 256u + x * 128u;   // O_X
+          ok = warp_wait(s_full(x), n & 1u, ab, kSiteEpiAccFull, lane);
+          // this thread's 64 columns of S: one Tensor Memory round trip
+          float v[2][32];
+          float mine = -INFINITY;
+          if (ok) {
+            tc_fence_after_sync();
+            mine = sc >= 0.0f ? half_row_max_scaled<false>(s_col + 64u * h, valid_h, sc, v)
+                              : half_row_max_scaled<true>(s_col + 64u * h, valid_h, sc, v);
+          }
+          const float other = exchange(mine, ok);
+          if (!ok) break;
+          float mx = x ? m_b : m_a, lx = x ? l_b : l_a;
+          const float m_blk = fmaxf(mine, other);  // key 0 is valid: finite
+          // both threads of a row take the same decisions from the same values
+          const bool grow = j > 0 && m_blk > mx + kAttnRescaleLog2;
+          if (j == 0) mx = m_blk;
+          if (__any_sync(0xffffffffu, grow)) {
+            // rescale this half of O_X and l by exp2(m_old - m_new) in the rows
+            // that need it (O_X is final for the previous block: see the header)
+            const float r = grow ? fast_exp2(mx - m_blk) : 1.0f;
+            if (grow) {
+              lx *= r;
+              mx = m_blk;
+            }
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+              float o[16];
+              const uint32_t oc = o_col + 64u * h + 16u * c;
+              tmem_ld_16cols(oc, o);
+              tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 16; e += 2) fma2(o[e], o[e + 1], o[e], o[e + 1], r, r, 0.0f, 0.0f);
-            tmem_st_16cols(o_col + 16u * c, o);
+              for (int e = 0; e < 16; e += 2) fma2(o[e], o[e + 1], o[e], o[e + 1], r, r, 0.0f, 0.0f);
+              tmem_st_16cols(oc, o);
+            }
+            tmem_wait_st();
+          }
+          // P as bf16 pairs: key k of the block into column kAttnPCol + k / 2 of
+          // S_X, so each thread writes only columns whose scores it has loaded
+          const float nm = -mx;
+          float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f, s3 = 0.0f;
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            float w[16];
+            exp_pack(v[c], 64 * static_cast<int>(h) + 32 * c, valid, sc, nm, w, s0, s1, s2, s3);
+            tmem_st_16cols(s_col + kAttnPCol + 32u * h + 16u * c, w);
+          }
+          // l sums the unrounded p: the bf16 rounding then perturbs only the
+          // numerator of O = (P V) / l, by at most 2^-8 sum_c p_c |V_c| / l
+          lx += (s0 + s1) + (s2 + s3);
+          if (x) {
+            m_b = mx;
+            l_b = lx;
+          } else {
+            m_a = mx;
+            l_a = lx;
           }
           tmem_wait_st();
-        }
-        // P over the first 64 columns of S_X (keys 32c..32c+31 into columns
-        // 16c..16c+15): every score is already in registers
-        const float nm = -m;
-        float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f, s3 = 0.0f;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          float w[16];
-          exp_pack(v[c], 32 * c, valid, sc, nm, w, s0, s1, s2, s3);
-          tmem_st_16cols(s_col + 16u * c, w);
-        }
-        // l sums the unrounded p: the bf16 rounding then perturbs only the
-        // numerator of O = (P V) / l, by at most 2^-8 sum_c p_c |V_c| / l
-        l += (s0 + s1) + (s2 + s3);
-        tmem_wait_st();
-        tc_fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(p_ready(x));
-      }
-      if (!ok) break;
-      // O_X / l for this row, once the item's last product has landed
-      if (!(ok = warp_wait(o_full(x), ti & 1u, ab, kSiteEpiAccFull, lane))) break;
-      tc_fence_after_sync();
-      const float inv = 1.0f / l;
-      __nv_bfloat16* dst = p.O + static_cast<int64_t>(b) * p.so + static_cast<int64_t>(qi) * p.ldo;
-#pragma unroll 1
-      for (int c = 0; c < 8; ++c) {
-        float o[16];
-        tmem_ld_16cols(o_col + 16u * c, o);
-        tmem_wait_ld();
-        if (c == 7) {  // O_X may take the next item
           tc_fence_before_sync();
           __syncwarp();
-          if (lane == 0) mbar_arrive(o_empty(x));
+          if (lane == 0) mbar_arrive(p_ready(x));
         }
-        if (qi < p.Lq) {
+      }
+      if (!ok) break;
+      // O_X / l for this row (this thread's 64 of its 128 columns), once the
+      // item's last product has landed
+#pragma unroll 1
+      for (uint32_t x = 0; x < 2; ++x) {
+        ok = warp_wait(o_full(x), ti & 1u, ab, kSiteEpiAccFull, lane);
+        const float lx = x ? l_b : l_a;
+        const float l_row = lx + exchange(lx, ok);  // the same sum in both threads
+        if (!ok) break;
+        tc_fence_after_sync();
+        const float inv = 1.0f / l_row;
+        const uint32_t o_col = tmem_base + lane_off + 256u + x * 128u + 64u * h;
+        const int qi = static_cast<int>(item % p.q_tiles) * kAttnItemRows + static_cast<int>(x) * kAttnM + row;
+        __nv_bfloat16* dst =
+            p.O + static_cast<int64_t>(b) * p.so + static_cast<int64_t>(qi) * p.ldo + 64 * static_cast<int>(h);
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          float o[16];
+          tmem_ld_16cols(o_col + 16u * c, o);
+          tmem_wait_ld();
+          if (c == 3) {  // O_X may take the next item
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(o_empty(x));
+          }
+          if (qi < p.Lq) {
 #pragma unroll
-          for (int d = 0; d < 16; d += 8) {
-            uint32_t wds[4];
+            for (int d = 0; d < 16; d += 8) {
+              uint32_t wds[4];
 #pragma unroll
-            for (int e2 = 0; e2 < 4; ++e2) {
-              const __nv_bfloat162 h2 =
-                  __floats2bfloat162_rn(o[d + 2 * e2] * inv, o[d + 2 * e2 + 1] * inv);
-              wds[e2] = *reinterpret_cast<const uint32_t*>(&h2);
+              for (int e2 = 0; e2 < 4; ++e2) {
+                const __nv_bfloat162 h2 =
+                    __floats2bfloat162_rn(o[d + 2 * e2] * inv, o[d + 2 * e2 + 1] * inv);
+                wds[e2] = *reinterpret_cast<const uint32_t*>(&h2);
+              }
+              *reinterpret_cast<uint4*>(dst + 16 * c + d) = make_uint4(wds[0], wds[1], wds[2], wds[3]);
             }
-            *reinterpret_cast<uint4*>(dst + 16 * c + d) = make_uint4(wds[0], wds[1], wds[2], wds[3]);
           }
         }
       }

@@ -109,6 +109,8 @@ SHAPES = [
     (1, 1, 1),         # the degenerate softmax over one key: O = V's row
     (2, 64, 1000),     # eight key blocks, the last 104 wide
     (1, 300, 129),     # a one-key last block
+    (1, 130, 64),      # one block of exactly the lower key half (the upper half holds none)
+    (2, 100, 65),      # one key in the upper half of the only block
 ]
 
 
