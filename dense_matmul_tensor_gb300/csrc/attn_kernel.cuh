@@ -143,6 +143,26 @@ __device__ __forceinline__ float extreme32(const float (&v)[32], int valid, floa
   return kMin ? fminf(a, b) : fmaxf(a, b);
 }
 
+// Extreme (kMin: smallest, else largest) of 64 scores: eight independent
+// chains of four steps, then two merge steps, so the longest dependent chain
+// is six instructions (one running extreme over all 64 would be 32).
+template <bool kMin>
+__device__ __forceinline__ float extreme64(const float (&v)[2][32]) {
+  float a[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int c = k >> 2, o = 2 * (k & 3);
+    a[k] = kMin ? fminf(v[c][o], v[c][o + 1]) : fmaxf(v[c][o], v[c][o + 1]);
+#pragma unroll
+    for (int i = 8; i < 32; i += 8)
+      a[k] = kMin ? min3(a[k], v[c][i + o], v[c][i + o + 1]) : max3(a[k], v[c][i + o], v[c][i + o + 1]);
+  }
+  const float x = kMin ? min3(a[0], a[1], a[2]) : max3(a[0], a[1], a[2]);
+  const float y = kMin ? min3(a[3], a[4], a[5]) : max3(a[3], a[4], a[5]);
+  const float z = kMin ? fminf(a[6], a[7]) : fmaxf(a[6], a[7]);
+  return kMin ? min3(x, y, z) : max3(x, y, z);
+}
+
 // Loads this thread's half row of an S block (64 columns at taddr) into `v`
 // with one wait, and returns the largest alpha * log2(e) * s over its valid
 // keys (-inf when the half holds none).  kMin: alpha < 0, so the smallest raw
@@ -153,6 +173,7 @@ __device__ __forceinline__ float half_row_max_scaled(uint32_t taddr, int valid, 
   tmem_ld_32cols(taddr, v[0]);
   tmem_ld_32cols(taddr + 32u, v[1]);
   tmem_wait_ld();
+  if (valid >= 64) return extreme64<kMin>(v) * sc;
   if (valid <= 0) return -INFINITY;
   float acc = kMin ? INFINITY : -INFINITY;
   acc = extreme32<kMin>(v[0], valid, acc);
@@ -165,32 +186,49 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
-// p = exp2(s * sc - m) for 32 keys of the row (key0 = their first index
-// within the block; keys from `valid` on are zero), summed into (s0..s3) and
-// packed as bf16 pairs (lower key in the low half) into 16 words.
-__device__ __forceinline__ void exp_pack(float (&v)[32], int key0, int valid, float sc, float nm,
-                                         float* w, float& s0, float& s1, float& s2, float& s3) {
+// p = exp2(s * sc - m) for the 64 keys of a half row (key0 = the first
+// one's index within the block; keys from `valid` on are zero), packed as
+// bf16 pairs (lower key in the low half) into w; returns their sum.  All 64
+// exponentials are independent and come before any packing, and the sum
+// runs in eight partial sums, so no long dependent chain stalls the warp.
+__device__ __forceinline__ float exp_pack64(float (&v)[2][32], int key0, int valid, float sc, float nm,
+                                            float (&w)[2][16]) {
 #pragma unroll
-  for (int e = 0; e < 32; e += 2) {
-    fma2(v[e], v[e + 1], v[e], v[e + 1], sc, sc, nm, nm);
-    v[e] = fast_exp2(v[e]);
-    v[e + 1] = fast_exp2(v[e + 1]);
-  }
-  if (valid < key0 + 32) {
+  for (int c = 0; c < 2; ++c) {
 #pragma unroll
-    for (int e = 0; e < 32; ++e)
-      if (key0 + e >= valid) v[e] = 0.0f;
+    for (int e = 0; e < 32; e += 2) {
+      fma2(v[c][e], v[c][e + 1], v[c][e], v[c][e + 1], sc, sc, nm, nm);
+      v[c][e] = fast_exp2(v[c][e]);
+      v[c][e + 1] = fast_exp2(v[c][e + 1]);
+    }
+  }
+  if (valid < key0 + 64) {
+#pragma unroll
+    for (int c = 0; c < 2; ++c)
+#pragma unroll
+      for (int e = 0; e < 32; ++e)
+        if (key0 + 32 * c + e >= valid) v[c][e] = 0.0f;
+  }
+  float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f, s3 = 0.0f, s4 = 0.0f, s5 = 0.0f, s6 = 0.0f, s7 = 0.0f;
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+#pragma unroll
+    for (int e = 0; e < 32; e += 8) {
+      add2(s0, s1, v[c][e], v[c][e + 1]);
+      add2(s2, s3, v[c][e + 2], v[c][e + 3]);
+      add2(s4, s5, v[c][e + 4], v[c][e + 5]);
+      add2(s6, s7, v[c][e + 6], v[c][e + 7]);
+    }
   }
 #pragma unroll
-  for (int e = 0; e < 32; e += 4) {
-    add2(s0, s1, v[e], v[e + 1]);
-    add2(s2, s3, v[e + 2], v[e + 3]);
-  }
+  for (int c = 0; c < 2; ++c) {
 #pragma unroll
-  for (int e = 0; e < 16; ++e) {
-    const __nv_bfloat162 h2 = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
-    w[e] = __uint_as_float(*reinterpret_cast<const uint32_t*>(&h2));
+    for (int e = 0; e < 16; ++e) {
+      const __nv_bfloat162 h2 = __floats2bfloat162_rn(v[c][2 * e], v[c][2 * e + 1]);
+      w[c][e] = __uint_as_float(*reinterpret_cast<const uint32_t*>(&h2));
+    }
   }
+  return ((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7));
 }
 
 __global__ void __launch_bounds__(kAttnThreads, 1)
@@ -455,17 +493,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           }
           // P as bf16 pairs: key k of the block into column kAttnPCol + k / 2 of
           // S_X, so each thread writes only columns whose scores it has loaded
-          const float nm = -mx;
-          float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f, s3 = 0.0f;
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            float w[16];
-            exp_pack(v[c], 64 * static_cast<int>(h) + 32 * c, valid, sc, nm, w, s0, s1, s2, s3);
-            tmem_st_16cols(s_col + kAttnPCol + 32u * h + 16u * c, w);
-          }
+          float w[2][16];
+          const float p_sum = exp_pack64(v, 64 * static_cast<int>(h), valid, sc, -mx, w);
+          tmem_st_16cols(s_col + kAttnPCol + 32u * h, w[0]);
+          tmem_st_16cols(s_col + kAttnPCol + 32u * h + 16u, w[1]);
           // l sums the unrounded p: the bf16 rounding then perturbs only the
           // numerator of O = (P V) / l, by at most 2^-8 sum_c p_c |V_c| / l
-          lx += (s0 + s1) + (s2 + s3);
+          lx += p_sum;
           if (x) {
             m_b = mx;
             l_b = lx;
