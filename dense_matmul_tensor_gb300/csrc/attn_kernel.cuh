@@ -64,6 +64,7 @@ constexpr uint32_t kAttnSmem = 1024 + 6 * kAttnTile + kAttnBarBytes + kAttnXchBy
 static_assert(kAttnSmem <= 232448, "shared memory per CTA");
 constexpr float kAttnRescaleLog2 = 8.0f;  // lazy-rescale threshold
 constexpr uint32_t kAttnPCol = 32;        // P_X's first column within S_X
+constexpr float kAttnSpecLog2 = 64.0f;    // bound on log2 p before the row maximum is known
 
 struct AttnParams {
   int32_t Lq, Lk;
@@ -186,13 +187,10 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
-// p = exp2(s * sc - m) for the 64 keys of a half row (key0 = the first
-// one's index within the block; keys from `valid` on are zero), packed as
-// bf16 pairs (lower key in the low half) into w; returns their sum.  All 64
-// exponentials are independent and come before any packing, and the sum
-// runs in eight partial sums, so no long dependent chain stalls the warp.
-__device__ __forceinline__ float exp_pack64(float (&v)[2][32], int key0, int valid, float sc, float nm,
-                                            float (&w)[2][16]) {
+// p = exp2(s * sc - m) in place for the 64 keys of a half row (key0 = the
+// first one's index within the block; keys from `valid` on are zero).  All
+// 64 exponentials are independent: nothing waits on one before the next.
+__device__ __forceinline__ void exp64(float (&v)[2][32], int key0, int valid, float sc, float nm) {
 #pragma unroll
   for (int c = 0; c < 2; ++c) {
 #pragma unroll
@@ -209,6 +207,18 @@ __device__ __forceinline__ float exp_pack64(float (&v)[2][32], int key0, int val
       for (int e = 0; e < 32; ++e)
         if (key0 + 32 * c + e >= valid) v[c][e] = 0.0f;
   }
+}
+
+__device__ __forceinline__ void scale64(float (&v)[2][32], float r) {
+#pragma unroll
+  for (int c = 0; c < 2; ++c)
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) fma2(v[c][e], v[c][e + 1], v[c][e], v[c][e + 1], r, r, 0.0f, 0.0f);
+}
+
+// Packs the 64 p of a half row as bf16 pairs (lower key in the low half) into
+// w and returns their sum (eight partial sums: short dependent chains).
+__device__ __forceinline__ float sum_pack64(const float (&v)[2][32], float (&w)[2][16]) {
   float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f, s3 = 0.0f, s4 = 0.0f, s5 = 0.0f, s6 = 0.0f, s7 = 0.0f;
 #pragma unroll
   for (int c = 0; c < 2; ++c) {
@@ -456,29 +466,35 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           const uint32_t s_col = tmem_base + lane_off + x * 128u;          // S_X
           const uint32_t o_col = tmem_base + lane_off + 256u + x * 128u;   // O_X
           ok = warp_wait(s_full(x), n & 1u, ab, kSiteEpiAccFull, lane);
+          float mx = x ? m_b : m_a, lx = x ? l_b : l_a;
           // this thread's 64 columns of S: one Tensor Memory round trip
           float v[2][32];
-          float mine = -INFINITY;
+          float mine = -INFINITY, m_use = 0.0f;
           if (ok) {
             tc_fence_after_sync();
             mine = sc >= 0.0f ? half_row_max_scaled<false>(s_col + 64u * h, valid_h, sc, v)
                               : half_row_max_scaled<true>(s_col + 64u * h, valid_h, sc, v);
+            // The exponentials start before the partner's maximum arrives:
+            // against the running maximum (raised if need be so that
+            // p <= 2^64), or in a row's first block against this half's own
+            // maximum.  Below, p moves to the row's common maximum where the
+            // two differ (p * exp2(m_use - m_new) = exp2(s - m_new)).
+            m_use = j == 0 ? mine : fmaxf(mx, mine - kAttnSpecLog2);
+            exp64(v, 64 * static_cast<int>(h), valid, sc, -m_use);
           }
           const float other = exchange(mine, ok);
           if (!ok) break;
-          float mx = x ? m_b : m_a, lx = x ? l_b : l_a;
           const float m_blk = fmaxf(mine, other);  // key 0 is valid: finite
           // both threads of a row take the same decisions from the same values
           const bool grow = j > 0 && m_blk > mx + kAttnRescaleLog2;
-          if (j == 0) mx = m_blk;
+          const float m_new = (j == 0 || grow) ? m_blk : mx;
+          if (__any_sync(0xffffffffu, m_use != m_new))
+            scale64(v, m_use == m_new ? 1.0f : fast_exp2(m_use - m_new));
           if (__any_sync(0xffffffffu, grow)) {
             // rescale this half of O_X and l by exp2(m_old - m_new) in the rows
             // that need it (O_X is final for the previous block: see the header)
-            const float r = grow ? fast_exp2(mx - m_blk) : 1.0f;
-            if (grow) {
-              lx *= r;
-              mx = m_blk;
-            }
+            const float r = grow ? fast_exp2(mx - m_new) : 1.0f;
+            if (grow) lx *= r;
 #pragma unroll 1
             for (int c = 0; c < 4; ++c) {
               float o[16];
@@ -491,10 +507,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             }
             tmem_wait_st();
           }
+          mx = m_new;
           // P as bf16 pairs: key k of the block into column kAttnPCol + k / 2 of
           // S_X, so each thread writes only columns whose scores it has loaded
           float w[2][16];
-          const float p_sum = exp_pack64(v, 64 * static_cast<int>(h), valid, sc, -mx, w);
+          const float p_sum = sum_pack64(v, w);
           tmem_st_16cols(s_col + kAttnPCol + 32u * h, w[0]);
           tmem_st_16cols(s_col + kAttnPCol + 32u * h + 16u, w[1]);
           // l sums the unrounded p: the bf16 rounding then perturbs only the
