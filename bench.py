@@ -311,16 +311,20 @@ def time_e2e(p, steps, warmup, stream, dev):
     return ms, h2d, d2h, chunks
 
 
-def grouped_measure(dev, stream, steps, count=1000, seed=7):
+def grouped_measure(dev, stream, steps, peaks, count=1000, seed=7):
     """Many small independent products (M, N, K drawn from 64..256, bf16 in,
     fp32 out): one grouped launch against one bmm_run per problem.  Both
-    are timed with CUDA events around the whole set on the same stream."""
+    are timed with CUDA events around the whole set on the same stream (back
+    to back: the set's operands, ~205 MB, exceed L2).  The set's arithmetic
+    intensity (~41 FLOP/byte) is far below the ridge, so the grouped launch
+    is also reported as GB/s of algorithmic bytes (A and B read, C written
+    once per problem) against the measured HBM copy bandwidth."""
     import torch
     from dense_matmul_tensor_gb300 import bmm
     rng = np.random.default_rng(seed)
     g = torch.Generator(device=dev)
     g.manual_seed(seed)
-    items, plans, flops = [], [], 0
+    items, plans, flops, nbytes = [], [], 0, 0
     for _ in range(count):
         M, N, K = (int(rng.choice([64, 128, 192, 256])) for _ in range(3))
         A = torch.randn(M * K, generator=g, device=dev).to(torch.bfloat16)
@@ -330,6 +334,7 @@ def grouped_measure(dev, stream, steps, count=1000, seed=7):
         plans.append(bmm.Plan(bmm.make_desc(batch=1, M=M, N=N, K=K, lda=K, ldb=N, ldc=N, strideA=0,
                                             strideB=0, strideC=0, typeA="bf16", typeC="f32")))
         flops += 2 * M * N * K
+        nbytes += 2 * M * K + 2 * K * N + 4 * M * N
     arr, n = bmm.make_problems(items)
     gplan = bmm.bmm_grouped_create(arr, n, 0, 0, "bf16", "f32")
     torch.cuda.synchronize()
@@ -354,13 +359,14 @@ def grouped_measure(dev, stream, steps, count=1000, seed=7):
         e1.record(stream)
         torch.cuda.synchronize()
         ms = e0.elapsed_time(e1) / reps
-        out[name] = {"ms": ms, "TFLOP/s": flops / (ms * 1e-3) / 1e12}
+        out[name] = {"ms": ms, "TFLOP/s": flops / (ms * 1e-3) / 1e12, "GB/s": nbytes / (ms * 1e-3) / 1e9}
     info = bmm.bmm_grouped_get_info(gplan)
     bmm.bmm_grouped_destroy(gplan)
     for pl in plans:
         pl.close()
     out.update({"workload": f"grouped_{count}_problems_64_to_256_bf16_f32", "problems": count,
-                "tiles": info["tiles"], "tile_n": info["tile_n"],
+                "tiles": info["tiles"], "tile_n": info["tile_n"], "algorithmic_bytes": nbytes,
+                "frac_hbm": out["grouped"]["GB/s"] / peaks["hbm_gbs"],
                 "speedup_vs_one_call_per_problem": out["one_call_per_problem"]["ms"] / out["grouped"]["ms"]})
     return out
 
@@ -644,7 +650,7 @@ def main():
         pair_ms = pair[qk] + pair[pv] if qk in pair and pv in pair else None
         line["fused_attention"] = fused_attention_measure(dev, stream, args.steps, flush, peaks,
                                                           pair_ms)
-        line["grouped"] = grouped_measure(dev, stream, args.steps)
+        line["grouped"] = grouped_measure(dev, stream, args.steps, peaks)
 
     if rank == 0 and not args.no_cpu:
         sampler = OracleSample(p)

@@ -152,6 +152,21 @@ def test_scale_sign_zero_and_sharp(alpha):
         assert np.allclose(O, mean[:, None, :], rtol=2.0 ** -7, atol=1e-3)
 
 
+@pytest.mark.parametrize("alpha", [1.0, -1.0])
+def test_a_later_block_far_above_the_running_maximum(alpha):
+    # keys 128..255 scaled by 2^6: block 1's scores exceed block 0's maximum
+    # by far more than 2^64 in log2 units, so its exponentials must be redone
+    # against its own maximum and O, l from block 0 rescale to (nearly) zero;
+    # block 2 falls back far below the new maximum
+    _need_gpu()
+    Q, K, V = wl.attention_qkv(2, 130, D, Lk=400, seed=71)
+    k = oracle.decode(K, "bf16").astype(np.float32)
+    k[:, 128:256, :] *= 64.0
+    K = (k.view(np.uint32) >> 16).astype(np.uint16)  # exact: a power-of-two scale
+    O = run_attn(Q, K, V, alpha=alpha)
+    check(O, Q, K, V, alpha)
+
+
 def test_repeat_runs_are_bitwise_identical():
     _need_gpu()
     Q, K, V = wl.attention_qkv(4, 256, D, Lk=384, seed=51)
