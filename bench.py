@@ -60,7 +60,7 @@ NCU_TRAFFIC = {
     ("fc08f5e59810500d", "gemm_4096x4096x4096_tn_bf16"): 85947392 + 17562368,
     # captured at batch 64 and scaled by 2 to the batch-128 launch (every query
     # tile does the same work); most of O's write-back happens after the kernel
-    ("3bfed907a0640253", "attn_fused_b128_2048x2048x128_bf16"): 2 * (100733440 + 5847552),
+    ("4be98bb27f03de4c", "attn_fused_b128_2048x2048x128_bf16"): 2 * (100733440 + 5847552),
 }
 
 # the sources each kernel family is built from

@@ -22,8 +22,8 @@
 //                 O_A += P_A(j) V_j, S_A(j+1), O_B += P_B(j) V_j, S_B(j+1)
 //               S_X = Q_X K_j^T (both operands K-major, from shared memory);
 //               P_X V_j reads P_X from Tensor Memory and V MN-major from
-//               shared memory.  While one warpgroup works on its scores the
-//               tensor core works on the other tile.
+//               shared memory.  While the softmax warps work on one tile's
+//               scores the tensor core works on the other tile.
 //   warps 2..9  softmax, all eight warps on tile A, then on tile B, per key
 //               block.  Warps w and w+4 share a Tensor Memory lane quarter and
 //               split each of its 32 rows: w takes keys 0..63 of the block,
@@ -54,7 +54,7 @@ constexpr int kAttnD = 128;        // head dimension (two 64-wide swizzle atoms)
 constexpr int kAttnM = 128;        // query rows per tile
 constexpr int kAttnItemRows = 256; // query rows per item: two tiles
 constexpr int kAttnN = 128;        // keys per block
-constexpr int kAttnThreads = 320;  // TMA warp, MMA warp, two softmax warpgroups
+constexpr int kAttnThreads = 320;  // TMA warp, MMA warp, eight softmax warps
 constexpr uint32_t kAttnHalf = 128u * 128u;       // one 64-column half of 128 rows: 16 KB
 constexpr uint32_t kAttnTile = 2u * kAttnHalf;    // Q, K or V tile: 32 KB
 constexpr uint32_t kAttnBarBytes = 256;
@@ -396,7 +396,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         if (ok && nb == 1) tc_commit(q_empty);  // Q is free once every S of the item is done
         for (int j = 0; j < nb && ok; ++j) {
           const uint32_t vs = gv & 1u, vph = (gv >> 1) & 1u;
-          // P_X(j) is warpgroup X's (ti * nb + j)-th block: every item has nb blocks
+          // P_X(j) is tile X's (ti * nb + j)-th block: every item has nb blocks
           const uint32_t pph = (ti * static_cast<uint32_t>(nb) + static_cast<uint32_t>(j)) & 1u;
           for (uint32_t x = 0; x < 2 && ok; ++x) {
             // V and O first, the softmax's release last: each wait costs the
