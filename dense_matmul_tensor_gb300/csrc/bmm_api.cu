@@ -198,7 +198,16 @@ void plan(const bmm_desc_t* d, Planned* P, int sms, bool row_loader) {
   P->tx_bytes = (P->a.pack == 2 ? 0u : P->a_bytes) + (P->b.pack == 2 ? 0u : b_bytes);
   const int64_t fixed = 1024 + dmt::kEpiBytes + dmt::kBarBytes;
   int stages = static_cast<int>((dmt::kSmemLimit - fixed) / P->stage_bytes);
-  if (stages > 16) stages = 16;
+  // At most 8 stages: only the narrow tiles (BN 16 and 32) fit more, and on the
+  // HBM-bound skinny product 8 in flight per SM measured 4% faster than 10
+  // (more outstanding loads than HBM serves well); 6, 5 and 4 were slower.
+  if (stages > dmt::kMaxStages) stages = dmt::kMaxStages;
+  // DMT_BMM_STAGES caps the ring depth (comparisons; at least 2)
+  const char* se = std::getenv("DMT_BMM_STAGES");
+  if (se && *se) {
+    const int cap = std::atoi(se);
+    if (cap >= 2 && cap < stages) stages = cap;
+  }
   P->stages = stages;
   P->smem_bytes = fixed + static_cast<int64_t>(stages) * P->stage_bytes;
 
@@ -836,7 +845,7 @@ bmm_status_t bmm_grouped_create(int32_t count, const bmm_group_problem_t* proble
   pl->tx_bytes = pl->a_bytes + b_bytes;
   const int64_t fixed = 1024 + dmt::kEpiBytes + dmt::kBarBytes;
   pl->stages = static_cast<int>((dmt::kSmemLimit - fixed) / pl->stage_bytes);
-  if (pl->stages > 16) pl->stages = 16;
+  if (pl->stages > dmt::kMaxStages) pl->stages = dmt::kMaxStages;
   pl->smem_bytes = fixed + static_cast<int64_t>(pl->stages) * pl->stage_bytes;
   uint32_t cols = 32;
   while (cols < static_cast<uint32_t>(2 * pl->bn)) cols <<= 1;

@@ -57,9 +57,14 @@ constexpr int kEpiPitch = 33; // floats per staged row (bank-conflict-free)
 // Epilogue staging, shared by the two store paths: four 32 x 33 fp32 tiles
 // (coalesced direct stores) or two 4 KB TMA-store boxes per epilogue warp.
 constexpr uint32_t kEpiBoxBytes = 4096u;
+constexpr int kMaxStages = 8;      // deepest operand ring the planner builds
 constexpr uint32_t kEpiBytes = 4u * 2u * kEpiBoxBytes;
 static_assert(kEpiBytes >= 4u * 32u * kEpiPitch * 4u, "direct-store staging must fit");
 constexpr uint32_t kBarBytes = 512;   // barriers, TMEM slot, abort flag
+// full[S], empty[S], two acc_full, two acc_empty, drain, then the TMEM slot and
+// the abort flag must end before byte 256 of the barrier block (the grouped
+// launches' schedule state starts there)
+static_assert(8u * (2u * kMaxStages + 5u) + 8u <= 256u, "barrier block layout");
 constexpr uint32_t kSmemLimit = 232448;  // 227 KB dynamic shared memory per CTA
 
 // Device error word: kErrTag | (site << 8) | role-specific detail.

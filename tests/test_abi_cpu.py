@@ -118,9 +118,13 @@ def test_planner_on_workloads(lib, name):
     assert info.stages >= 4
     assert info.tmem_cols >= 2 * info.tile_n and info.tmem_cols <= 512
     assert info.even_k == (p.K % 64 == 0)
+    assert info.stages <= 8
     if p is wl.SKINNY:
         assert info.swap_ab == 1 and info.tile_n == 16
         assert info.tiles == p.batch * 2          # N=256 over two 128-row MMA tiles
+        # 18 KB stages would fit ten deep; eight measured faster on this
+        # HBM-bound shape, and the planner builds at most eight
+        assert info.stages == 8
     if p is wl.GEMM_4096:
         # CTA pairs with 256 x 224 tiles: 16 x 19 = 304 tiles = exactly 4 rounds
         # on 76 pairs (256-wide tiles would leave a 0.37 wave); 30 KB per CTA
@@ -146,6 +150,16 @@ def test_planner_boundary_shapes(lib):
                                         strideA=M * 48, strideB=48 * 96, strideC=M * 96))
         assert info.even_k == 0
         assert info.tiles >= 1
+
+
+def test_stage_cap_from_the_environment(lib, monkeypatch):
+    monkeypatch.setenv("DMT_BMM_STAGES", "4")
+    info = api.bmm_plan_query(desc_for(wl.GEMM_4096))
+    assert info.stages == 4 and info.smem_bytes <= SMEM_LIMIT
+    monkeypatch.setenv("DMT_BMM_STAGES", "1")     # below 2: ignored
+    assert api.bmm_plan_query(desc_for(wl.GEMM_4096)).stages == 6
+    monkeypatch.setenv("DMT_BMM_STAGES", "12")    # above what the planner builds: ignored
+    assert api.bmm_plan_query(desc_for(wl.SKINNY)).stages == 8
 
 
 def test_pair_mode_can_be_switched_off(lib, monkeypatch):
