@@ -838,6 +838,13 @@ bmm_status_t bmm_grouped_create(int32_t count, const bmm_group_problem_t* proble
   pl->timeout_ns = wait_timeout_ns();
   // One tile shape for the launch: the smallest of 64/128/256 covering the widest N.
   pl->bn = max_n <= 64 ? 64 : (max_n <= 128 ? 128 : 256);
+  // DMT_BMM_TILE_N=64|128|256 pins the launch's tile width (comparisons); a
+  // problem wider than the tile takes several N tiles
+  const char* te = std::getenv("DMT_BMM_TILE_N");
+  if (te && *te) {
+    const int w = std::atoi(te);
+    if (w == 64 || w == 128 || w == 256) pl->bn = w;
+  }
   const int a_mn = transA ? 1 : 0, b_mn = transB ? 0 : 1;
   pl->a_bytes = static_cast<uint32_t>(dmt::kTileM * dmt::kTileK * 2);
   const uint32_t b_bytes = static_cast<uint32_t>(pl->bn * dmt::kTileK * 2);
