@@ -257,7 +257,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   volatile uint32_t* abort_flag = tmem_slot + 1;
 
   // barriers (8 bytes each); X = tile A (0) or B (1)
-  const uint32_t q_full = bar0, q_empty = bar0 + 8;
+  // Q_X of the item landed / free again (one pair per tile, so Q_A of the next
+  // item loads as soon as the item's last S_A is done)
+  auto q_full = [&](uint32_t x) { return x ? bar0 + 152 : bar0; };
+  auto q_empty = [&](uint32_t x) { return x ? bar0 + 160 : bar0 + 8; };
   auto k_full = [&](uint32_t s) { return bar0 + 16 + 8 * s; };
   auto k_empty = [&](uint32_t s) { return bar0 + 32 + 8 * s; };
   auto v_full = [&](uint32_t s) { return bar0 + 48 + 8 * s; };
@@ -272,8 +275,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
-    mbar_init(q_empty, 1);
+    for (uint32_t x = 0; x < 2; ++x) {
+      mbar_init(q_full(x), 1);
+      mbar_init(q_empty(x), 1);
+    }
     for (uint32_t s = 0; s < 2; ++s) {
       mbar_init(k_full(s), 1);
       mbar_init(k_empty(s), 1);
@@ -321,12 +326,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       for (int64_t item = blockIdx.x; item < p.items && ok; item += gridDim.x, ++ti) {
         const int b = static_cast<int>(item / p.q_tiles);
         const int q0 = static_cast<int>(item % p.q_tiles) * kAttnItemRows;
-        if (!wait_bounded<true>(q_empty, (ti & 1u) ^ 1u, ab, kSiteProducerEmpty)) break;
-        mbar_arrive_expect_tx(q_full, 2 * kAttnTile);
-        tma_load_3d(q_addr, &tmQ, q_full, 0, q0, b);
-        tma_load_3d(q_addr + kAttnHalf, &tmQ, q_full, 64, q0, b);
-        tma_load_3d(q_addr + kAttnTile, &tmQ, q_full, 0, q0 + kAttnM, b);
-        tma_load_3d(q_addr + kAttnTile + kAttnHalf, &tmQ, q_full, 64, q0 + kAttnM, b);
+        for (uint32_t x = 0; x < 2 && ok; ++x) {
+          if (!wait_bounded<true>(q_empty(x), (ti & 1u) ^ 1u, ab, kSiteProducerEmpty)) {
+            ok = false;
+            break;
+          }
+          const uint32_t qx = q_addr + x * kAttnTile;
+          mbar_arrive_expect_tx(q_full(x), kAttnTile);
+          tma_load_3d(qx, &tmQ, q_full(x), 0, q0 + static_cast<int>(x) * kAttnM, b);
+          tma_load_3d(qx + kAttnHalf, &tmQ, q_full(x), 64, q0 + static_cast<int>(x) * kAttnM, b);
+        }
+        if (!ok) break;
         // K_j, then V_{j-1}: a K slot frees as soon as both S of its block are done
         for (int j = 0; j < nb && ok; ++j) {
           const uint32_t s = gk & 1u;
@@ -345,7 +355,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       // let this CTA's last loads land before it can exit
       for (uint32_t j = gk > 2u ? gk - 2u : 0u; j < gk; ++j) drain_wait(k_full(j & 1u), (j >> 1) & 1u);
       for (uint32_t j = gv > 2u ? gv - 2u : 0u; j < gv; ++j) drain_wait(v_full(j & 1u), (j >> 1) & 1u);
-      if (ti > 0) drain_wait(q_full, (ti - 1) & 1u);
+      if (ti > 0) {
+        drain_wait(q_full(0), (ti - 1) & 1u);
+        drain_wait(q_full(1), (ti - 1) & 1u);
+      }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA
@@ -391,9 +404,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         (!first || ks > 0) ? 1u : 0u);
       };
       for (int64_t item = blockIdx.x; item < p.items && ok; item += gridDim.x, ++ti) {
-        if (!wait_bounded<true>(q_full, ti & 1u, ab, kSiteMmaFull)) break;
-        ok = issue_s_pair_half(0u) && issue_s_pair_half(1u);
-        if (ok && nb == 1) tc_commit(q_empty);  // Q is free once every S of the item is done
+        // Q_X is free once the item's last S_X is done
+        for (uint32_t x = 0; x < 2 && ok; ++x) {
+          ok = wait_bounded<true>(q_full(x), ti & 1u, ab, kSiteMmaFull) && issue_s_pair_half(x);
+          if (ok && nb == 1) tc_commit(q_empty(x));
+        }
         for (int j = 0; j < nb && ok; ++j) {
           const uint32_t vs = gv & 1u, vph = (gv >> 1) & 1u;
           // P_X(j) is tile X's (ti * nb + j)-th block: every item has nb blocks
@@ -417,7 +432,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             if (x == 1) tc_commit(v_empty(vs));
             if (j + 1 < nb) {
               if (!(ok = issue_s_pair_half(x))) break;
-              if (x == 1 && j + 2 == nb) tc_commit(q_empty);
+              if (j + 2 == nb) tc_commit(q_empty(x));
             }
           }
           ++gv;
