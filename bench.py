@@ -60,9 +60,7 @@ NCU_TRAFFIC = {
     ("a8b32a91d092e904", "gemm_4096x4096x4096_tn_bf16"): 85930752 + 17278976,
     # captured at batch 64 and scaled by 2 to the batch-128 launch (every query
     # tile does the same work); most of O's write-back happens after the kernel
-    # (captured before the operand-ring cap entered the shared header; the
-    # attention kernel does not use it)
-    ("99861c22d39c21cc", "attn_fused_b128_2048x2048x128_bf16"): 2 * (100733440 + 5847552),
+    ("a41fed3500d03539", "attn_fused_b128_2048x2048x128_bf16"): 2 * (100784640 + 6201344),
 }
 
 # the sources each kernel family is built from
