@@ -111,7 +111,8 @@ typedef struct bmm_plan_s* bmm_plan_t;
 /*
  * Validate `desc` and plan the product: tile shape by shape class (including
  * the swap to C^T for skinny M), ring depth from the shared-memory budget
- * (stages x (A tile + B tile), "Optimize Triton Block Parameters", Step 2),
+ * (stages x (A tile + B tile), "Optimize Triton Block Parameters", Step 2;
+ * at most 8, fewer with DMT_BMM_STAGES),
  * and, per operand, whether TMA reads it in place or it is first copied into
  * an aligned workspace (TMA needs 16-byte strides and bases; "FLA Triton ->
  * Gluon porting", section 3, TMA).
