@@ -12,7 +12,8 @@ evict L2; the flush is outside the timed interval.
 
 Prints one JSON line (rank 0).  ``roofline`` compares the dominant kernel's
 algorithmic FLOP/s (2*M*N*K per launch over its CUDA-event duration) with the
-measured dense bf16 peak; ``e2e`` repeats the metric with host buffers (H2D of
+measured dense bf16 peak (``frac_of_nominal``: against the nominal 2.25
+PFLOP/s; median and best launch times beside the mean); ``e2e`` repeats the metric with host buffers (H2D of
 A and B from pinned memory, the call, D2H of C inside each timed step);
 ``cpu_baseline`` times the fp64 oracle on the host cores on a bounded sample
 of the same workload.  ``other_workloads`` reports the remaining specified
@@ -51,6 +52,9 @@ import numpy as np  # noqa: E402
 MEASURED_FALLBACK = {"hbm_gbs": 6676.5, "bf16_tflops": 1932.9, "bf16_tflops_sustained": 1743.9,
                      "sm_max_mhz": 2070.0}
 RECIPE_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# Nominal GB300 figures (dense bf16 tensor rate, HBM3e bandwidth), reported
+# beside the measured denominators as a second fraction
+NOMINAL = {"hbm_gbs": 7900.0, "bf16_tflops": 2250.0}
 
 # DRAM traffic per launch of the dominant kernel from one ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum; profiles/ has the summary),
@@ -587,7 +591,9 @@ def main():
                        else f"bmm_tc_kernel<{info.tile_n}>"),
             "peak_source": f"{peak_src} " + ("bf16 burst" if tensor_bound else "HBM copy"),
             **per_launch,
-            "ms_per_launch_median": statistics.median(ms_list)}
+            "frac_of_nominal": achieved / (NOMINAL["bf16_tflops"] if tensor_bound else NOMINAL["hbm_gbs"]),
+            "ms_per_launch_median": statistics.median(ms_list),
+            "ms_per_launch_best": min(ms_list)}
 
     line = {"metric": METRIC,
             "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
