@@ -12,8 +12,10 @@ evict L2; the flush is outside the timed interval.
 
 Prints one JSON line (rank 0).  ``roofline`` compares the dominant kernel's
 algorithmic FLOP/s (2*M*N*K per launch over its CUDA-event duration) with the
-measured dense bf16 peak (``frac_of_nominal``: against the nominal 2.25
-PFLOP/s; median and best launch times beside the mean); ``e2e`` repeats the metric with host buffers (H2D of
+measured dense bf16 peak (``MEASURED_PEAKS.json``: cuBLAS bf16 burst), with
+ncu's tensor-pipe activity of the same kernel source beside it (null once the
+sources change) and the median and best launch times beside the mean;
+``e2e`` repeats the metric with host buffers (H2D of
 A and B from pinned memory, the call, D2H of C inside each timed step);
 ``cpu_baseline`` times the fp64 oracle on the host cores on a bounded sample
 of the same workload.  ``other_workloads`` reports the remaining specified
@@ -52,19 +54,23 @@ import numpy as np  # noqa: E402
 MEASURED_FALLBACK = {"hbm_gbs": 6676.5, "bf16_tflops": 1932.9, "bf16_tflops_sustained": 1743.9,
                      "sm_max_mhz": 2070.0}
 RECIPE_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-# Nominal GB300 figures (dense bf16 tensor rate, HBM3e bandwidth), reported
-# beside the measured denominators as a second fraction
-NOMINAL = {"hbm_gbs": 7900.0, "bf16_tflops": 2250.0}
 
 # DRAM traffic per launch of the dominant kernel from one ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum; profiles/ has the summary),
 # keyed by a hash of that kernel's sources and the workload: reported only
 # while those sources are unchanged.
 NCU_TRAFFIC = {
-    ("a8b32a91d092e904", "gemm_4096x4096x4096_tn_bf16"): 85930752 + 17278976,
+    ("198c4f16fad3679c", "gemm_4096x4096x4096_tn_bf16"): 85930752 + 17278976,
     # captured at batch 64 and scaled by 2 to the batch-128 launch (every query
     # tile does the same work); most of O's write-back happens after the kernel
     ("a41fed3500d03539", "attn_fused_b128_2048x2048x128_bf16"): 2 * (100784640 + 6201344),
+}
+# Tensor-pipe activity of the same captures (sm__pipe_tensor_cycles_active,
+# % of elapsed cycles): the hardware's own measure of how busy the tensor
+# cores were, reported beside the fraction of the measured cuBLAS peak.
+NCU_TENSOR_ACTIVE_PCT = {
+    ("198c4f16fad3679c", "gemm_4096x4096x4096_tn_bf16"): 71.50,
+    ("a41fed3500d03539", "attn_fused_b128_2048x2048x128_bf16"): 40.78,
 }
 
 # the sources each kernel family is built from
@@ -421,6 +427,8 @@ def fused_attention_measure(dev, stream, steps, flush, peaks, pair_ms=None, batc
            "roofline": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"],
                         "unit": "TFLOP/s", "frac": tf / peaks["bf16_tflops"],
                         "traffic": NCU_TRAFFIC.get((kernel_source_hash(ATTN_SOURCES), name)),
+                        "ncu_tensor_pipe_active_pct": NCU_TENSOR_ACTIVE_PCT.get(
+                            (kernel_source_hash(ATTN_SOURCES), name)),
                         "algorithmic_flops_per_launch": flops,
                         "algorithmic_bytes_per_launch": nbytes},
            "kernel": "attn_fwd_kernel", "launches_per_step": 1}
@@ -591,7 +599,7 @@ def main():
                        else f"bmm_tc_kernel<{info.tile_n}>"),
             "peak_source": f"{peak_src} " + ("bf16 burst" if tensor_bound else "HBM copy"),
             **per_launch,
-            "frac_of_nominal": achieved / (NOMINAL["bf16_tflops"] if tensor_bound else NOMINAL["hbm_gbs"]),
+            "ncu_tensor_pipe_active_pct": NCU_TENSOR_ACTIVE_PCT.get((kernel_source_hash(), p.name)),
             "ms_per_launch_median": statistics.median(ms_list),
             "ms_per_launch_best": min(ms_list)}
 

@@ -649,6 +649,38 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocWordByt
 std::mutex g_noalloc_mu;
 unsigned char* g_noalloc_addr[kNoAllocMaxDevices];
 
+// Co-resident CTA pairs per (device, tile width, shared memory), remembered
+// from the first call that launched the pair kernel with them, so later calls
+// skip the occupancy query (a plan keeps this number; these calls have none).
+struct NoAllocPairs {
+  int dev;
+  int tile_n;
+  int64_t smem;
+  int pairs;
+};
+constexpr int kNoAllocPairSlots = 64;
+NoAllocPairs g_noalloc_pairs[kNoAllocPairSlots];
+int g_noalloc_pairs_used = 0;
+
+int noalloc_cached_pairs(int dev, const Planned& P) {
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  for (int i = 0; i < g_noalloc_pairs_used; ++i)
+    if (g_noalloc_pairs[i].dev == dev && g_noalloc_pairs[i].tile_n == P.bn &&
+        g_noalloc_pairs[i].smem == P.smem_bytes)
+      return g_noalloc_pairs[i].pairs;
+  return 0;
+}
+
+void noalloc_remember_pairs(int dev, const Planned& P, int pairs) {
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  for (int i = 0; i < g_noalloc_pairs_used; ++i)
+    if (g_noalloc_pairs[i].dev == dev && g_noalloc_pairs[i].tile_n == P.bn &&
+        g_noalloc_pairs[i].smem == P.smem_bytes)
+      return;
+  if (g_noalloc_pairs_used < kNoAllocPairSlots)
+    g_noalloc_pairs[g_noalloc_pairs_used++] = NoAllocPairs{dev, P.bn, P.smem_bytes, pairs};
+}
+
 // Device address of the scratch array on device `dev` (which must be
 // current).  Looked up with cudaGetSymbolAddress on the first call per device.
 bmm_status_t noalloc_scratch(int dev, unsigned char** out) {
@@ -696,11 +728,14 @@ extern "C" bmm_status_t bmm_run_noalloc(const bmm_desc_t* desc, const void* A, c
   pl.err = reinterpret_cast<uint32_t*>(scratch);
   pl.ws = scratch + kNoAllocWordBytes;
 
+  if (pl.P.pair) pl.max_pairs = noalloc_cached_pairs(dev, pl.P);
+
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // The array keeps the previous call's contents: the error word must start at zero.
   if (cudaMemsetAsync(pl.err, 0, sizeof(uint32_t), s) != cudaSuccess) return BMM_ERR_CUDA;
   const bmm_status_t rst = bmm_run(&pl, A, B, C, alpha, beta, stream);
   if (rst != BMM_OK) return rst;
+  if (pl.P.pair && pl.max_pairs > 0) noalloc_remember_pairs(dev, pl.P, pl.max_pairs);
   if (device_error &&
       cudaMemcpyAsync(device_error, pl.err, sizeof(uint32_t), cudaMemcpyDeviceToDevice, s) !=
           cudaSuccess)

@@ -321,7 +321,10 @@ BMM_API bmm_status_t bmm_host_destroy(bmm_host_plan_t plan);
  *
  * The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call
- * before any stream capture.  Every call shares the array and it keeps the
+ * before any stream capture.  The address is kept for the life of the
+ * process: after a reset of the device (cudaDeviceReset, or any teardown of
+ * its primary context) it is stale, so do not call this entry point again in
+ * a process that has reset the device.  Every call shares the array and it keeps the
  * last call's contents, so calls whose work overlaps on the GPU (other
  * streams, other host threads) race on it: serialise them.  The error word
  * is cleared on `stream` at the start of each call.  If `device_error` is a

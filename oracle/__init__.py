@@ -179,12 +179,74 @@ def attention(Q, Kmat, V, *, batch, Lq, Lk, D, alpha, threads=None, want_bound=T
     return O, bnd
 
 
-def attention_tolerance(o_ref, bnd):
-    """Acceptance bound for the fused attention path per element: the
-    probabilities are rounded to bf16 before the P.V product (relative error
-    2^-8 each, so at most 2^-8 * sum_c p_ic |V_cd| in total, plus the fp32
-    sums), and O is rounded to bf16 once (2^-8 * |O|)."""
-    return 2.0 ** -7 * bnd + 2.0 ** -8 * np.abs(o_ref) + 1e-6
+def bf16_values(bits):
+    """bf16 bit patterns to float32 values: a bf16 pattern is the upper half
+    of the binary32 pattern of the same value, so widening is exact."""
+    b = np.ascontiguousarray(bits, dtype=np.uint16)
+    return (b.astype(np.uint32) << 16).view(np.float32)
+
+
+def _rows_max(bits, D, fn, chunk_rows=1 << 20):
+    """max over rows of fn(row values) for a [rows, D] bf16 bit array, in
+    chunks of rows (the key count may run to millions)."""
+    rows = bits.reshape(-1, D)
+    out = None
+    for r0 in range(0, rows.shape[0], chunk_rows):
+        v = fn(bf16_values(rows[r0:r0 + chunk_rows]).astype(np.float64))
+        m = v.max(axis=0)
+        out = m if out is None else np.maximum(out, m)
+    return out
+
+
+ATTN_ROUND = 2.0 ** -8   # one RNE rounding to bf16 (8-bit significand), relative
+ATTN_FP32 = 2.0 ** -14   # every fp32 step of the softmax and its sums, relative (see below)
+STATED_FP32 = 1e-5       # the stated fp32 accumulation allowance, relative to sum |a||b|
+
+
+def attention_tolerance(o_ref, bnd, Q, K, V, *, alpha):
+    """Acceptance bound per element of the fused attention form
+    O = softmax(alpha Q K^T) V, derived from the arithmetic it is held to
+    (scores accumulated in fp32, probabilities p rounded to bf16 before the
+    product with V, that product and the normaliser l = sum_c p_c summed in
+    fp32 from the unrounded p, O rounded to bf16 once):
+
+        tol = (2^-8 + eps + eta_i) * (B_id + |O_id|) + Lk * 2^-126 * max_c |V_cd|
+
+    with B_id = sum_c p_ic |V_cd| (the oracle's bound; p normalised).
+
+    * 2^-8 * B: each p_c moves by at most 2^-8 relative when rounded to bf16;
+      only the numerator sum_c p_c V_c sees that rounding (l sums the
+      unrounded p), so O moves by at most 2^-8 * B.
+    * 2^-8 * |O|: the one rounding of O to bf16.
+    * eta_i = |alpha| * 1e-5 * ||q_i||_2 * max_c ||k_c||_2: the stated fp32
+      product allowance (1e-5 * sum_k |q_k||k_ck|, bounded by Cauchy-Schwarz)
+      applied to each score; a score error ds scales p_c by exp(alpha ds),
+      and weights w_c perturbed by relative errors eta_c move
+      sum_c w_c V_c / sum_c w_c by at most max eta * (B + |O|).
+    * eps = 2^-14 covers the remaining fp32 steps, all far smaller: the same
+      1e-5 allowance for the P.V accumulation (relative to B) and for the sum
+      l (relative to |O|), the rounding of the exponent argument and of the
+      exponentials, the rescale products and the reciprocal of l (each a few
+      units of 2^-24 for the weights that matter), and the second-order term
+      2^-8 * 2^-8 * B of rounding an O that already carries the p error.
+    * Lk * 2^-126 * max|V|: probabilities below 2^-126 may be flushed to zero
+      (relative to a largest p of at least 1, so l >= 1).
+
+    Q is [batch, Lq, D] (the query rows of o_ref), K and V [batch, Lk, D]
+    (or flat), all bf16 bit patterns."""
+    o_ref = np.asarray(o_ref)
+    batch, Lq, D = o_ref.shape
+    Qb = np.asarray(Q).reshape(batch, Lq, D)
+    Kb = np.asarray(K).reshape(batch, -1, D)
+    Vb = np.asarray(V).reshape(batch, -1, D)
+    Lk = Kb.shape[1]
+    qn = np.sqrt(np.square(bf16_values(Qb).astype(np.float64)).sum(axis=2))      # [batch, Lq]
+    kn = np.array([_rows_max(Kb[b], D, lambda v: np.sqrt(np.square(v).sum(axis=1)))
+                   for b in range(batch)]).reshape(batch)                         # [batch]
+    vmax = np.array([_rows_max(Vb[b], D, np.abs) for b in range(batch)]).reshape(batch, D)
+    eta = abs(float(alpha)) * STATED_FP32 * qn * kn[:, None]
+    rel = ATTN_ROUND + ATTN_FP32 + eta[:, :, None]
+    return rel * (np.asarray(bnd) + np.abs(o_ref)) + Lk * 2.0 ** -126 * vmax[:, None, :]
 
 
 def round_bf16(x):

@@ -7,6 +7,8 @@ NaN in C, and a write outside C changes the sentinel.
 """
 from __future__ import annotations
 
+import dataclasses
+
 import numpy as np
 import torch
 
@@ -43,15 +45,15 @@ def decode_c(host: np.ndarray, p: wl.Problem) -> np.ndarray:
     """Dense float64 [batch, M, N] view of the C storage (host copy)."""
     s = p.strides()
     if p.type_c == "f32":
-        vals = host.astype(np.float64)
+        vals = np.ascontiguousarray(host, dtype=np.float32)
     else:
-        vals = torch.from_numpy(host.view(np.int16)).view(torch.bfloat16).double().numpy()
-    out = np.empty((p.batch, p.M, p.N), dtype=np.float64)
-    for b in range(p.batch):
-        for i in range(p.M):
-            o = b * s["sC"] + i * s["ldc"]
-            out[b, i] = vals[o:o + p.N]
-    return out
+        vals = torch.from_numpy(np.ascontiguousarray(host).view(np.int16)).view(torch.bfloat16).float().numpy()
+    if p.batch == 0 or p.M == 0 or p.N == 0:
+        return np.empty((p.batch, p.M, p.N), dtype=np.float64)
+    it = vals.itemsize
+    view = np.lib.stride_tricks.as_strided(vals, shape=(p.batch, p.M, p.N),
+                                           strides=(s["sC"] * it, s["ldc"] * it, it), writeable=False)
+    return view.astype(np.float64)
 
 
 def c_storage(p: wl.Problem, x: wl.Inputs, c_fill: str):
@@ -106,38 +108,109 @@ def run_gpu(p: wl.Problem, x: wl.Inputs, *, guard=4096, c_fill="nan", stream=Non
     return out[guard:guard + chost.size].copy(), info
 
 
-def check_full(p: wl.Problem, x: wl.Inputs, c_host: np.ndarray, *, exact=False):
-    """Element-by-element comparison with the full oracle."""
-    c_ref, bnd = oracle.bmm(x.A, x.B, x.C_in, **p.oracle_kwargs())
+def _batch_slice(p: wl.Problem, x: wl.Inputs, c_host: np.ndarray, b0: int, b1: int):
+    """Problem, inputs and C storage of batch items [b0, b1) of ``p``: the
+    same strides, the buffers cut at item b0 (a broadcast operand, batch
+    stride 0, is passed whole)."""
+    s = p.strides()
+    sub = dataclasses.replace(p, batch=b1 - b0, **s)
+    na, nb, nc = sub.storage_elems()
+    a0 = 0 if s["sA"] == 0 else b0 * s["sA"]
+    bb0 = 0 if s["sB"] == 0 else b0 * s["sB"]
+    c0 = b0 * s["sC"]
+    xs = wl.Inputs(x.A[a0:a0 + na], x.B[bb0:bb0 + nb],
+                   None if x.C_in is None else x.C_in[c0:c0 + nc])
+    return sub, xs, c_host[c0:c0 + nc]
+
+
+def check_full(p: wl.Problem, x: wl.Inputs, c_host: np.ndarray, *, exact=False,
+               max_elems=1 << 26):
+    """Element-by-element comparison of every element of C with the full
+    oracle, and no NaN or Inf anywhere in C.  Large problems are compared in
+    slices of whole batch items (at most ``max_elems`` outputs each, one
+    item at least) so the fp64 reference never has to fit in memory at once.
+    Returns the largest err/tol over all elements (0 for exact checks)."""
+    per_item = max(1, p.M * p.N)
+    step = max(1, max_elems // per_item)
+    worst = 0.0
+    for b0 in range(0, max(p.batch, 1), step):
+        b1 = min(p.batch, b0 + step)
+        if b1 <= b0:
+            break
+        sub, xs, cs = (p, x, c_host) if (b0 == 0 and b1 == p.batch) else _batch_slice(p, x, c_host, b0, b1)
+        worst = max(worst, _check_full_once(sub, xs, cs, exact=exact, item0=b0))
+    return worst
+
+
+def _check_full_once(p: wl.Problem, x: wl.Inputs, c_host: np.ndarray, *, exact, item0):
+    c_ref, bnd = oracle.bmm(x.A, x.B, x.C_in, want_bound=not exact, **p.oracle_kwargs())
     got = decode_c(c_host, p)
     assert np.all(np.isfinite(got)), "non-finite values in C"
     if exact:
         bad = got != c_ref
-        assert not bad.any(), f"{bad.sum()} elements differ from the exact result"
+        if bad.any():
+            idx = np.argwhere(bad)[:5]
+            raise AssertionError(f"{bad.sum()} elements differ from the exact result; first (b,i,j) "
+                                 f"{[(int(i[0]) + item0, int(i[1]), int(i[2])) for i in idx]}")
         return 0.0
-    cin = None if x.C_in is None else decode_c(x.C_in if p.type_c == "f32" else x.C_in, p)
+    cin = None if x.C_in is None else decode_c(x.C_in, p)
     tol = oracle.tolerance(c_ref, bnd, cin, alpha=p.alpha, beta=p.beta, out_bf16=p.type_c == "bf16")
+    del bnd, cin
     err = np.abs(got - c_ref)
     bad = err > tol
     if bad.any():
         idx = np.argwhere(bad)[:5]
         raise AssertionError(f"{bad.sum()} of {bad.size} elements outside tolerance; first "
-                             f"{[(tuple(i), got[tuple(i)], c_ref[tuple(i)], tol[tuple(i)]) for i in idx]}")
-    return float(np.max(err / np.maximum(tol, 1e-300))) if err.size else 0.0
+                             f"{[((int(i[0]) + item0, int(i[1]), int(i[2])), got[tuple(i)], c_ref[tuple(i)], tol[tuple(i)]) for i in idx]}")
+    if not err.size:
+        return 0.0
+    np.divide(err, np.maximum(tol, 1e-300), out=err)
+    return float(err.max())
 
 
-def sample_indices(p: wl.Problem, n: int, seed: int, tile_n: int = 256) -> np.ndarray:
-    """Random samples plus the corners and tile edges of every kind."""
+def _seams(extent: int, tile: int) -> set:
+    """Indices on both sides of every tile boundary below ``extent``, plus
+    the first and last index and the first index of the last (possibly
+    partial) tile."""
+    out = {0, extent - 1}
+    if tile > 0:
+        for t in range(tile, extent, tile):
+            out.update((t - 1, t))
+        out.add(((extent - 1) // tile) * tile)
+    return {v for v in out if 0 <= v < extent}
+
+
+def sample_indices(p: wl.Problem, n: int, seed: int, *, tile_m: int = 128,
+                   tile_n: int = 256, max_seams: int = 64) -> np.ndarray:
+    """Random samples plus the corners and the seams of the tiles the plan
+    actually uses (``tile_m`` rows, ``tile_n`` columns of C; for the swapped
+    form pass the tile extents of C's transpose swapped back), on the first
+    and last batch item.  At most ``max_seams`` seam indices per dimension
+    (evenly spread) keep the set small on large outputs."""
     rng = np.random.default_rng(seed)
     idx = [np.stack([rng.integers(0, p.batch, n), rng.integers(0, p.M, n),
                      rng.integers(0, p.N, n)], axis=1)]
-    edges_m = sorted({0, p.M - 1, *[m for m in (127, 128, 129, 255, 256) if m < p.M]})
-    edges_n = sorted({0, p.N - 1, *[v for v in (15, 16, 63, 64, 127, 128, 255, 256) if v < p.N]})
+
+    def thin(v):
+        v = sorted(v)
+        if len(v) <= max_seams:
+            return v
+        keep = np.unique(np.linspace(0, len(v) - 1, max_seams).round().astype(int))
+        return [v[k] for k in keep] + v[-2:]
+
+    edges_m = thin(_seams(p.M, tile_m))
+    edges_n = thin(_seams(p.N, tile_n))
     for b in {0, p.batch - 1}:
-        for i in edges_m:
-            for j in edges_n:
-                idx.append(np.array([[b, i, j]]))
+        grid = np.array([[b, i, j] for i in edges_m for j in edges_n], dtype=np.int64)
+        idx.append(grid)
     return np.concatenate(idx, axis=0).astype(np.int64)
+
+
+def plan_tiles(info):
+    """(tile_m, tile_n) of C from a plan's info (the plan reports the MMA
+    view, which for the swapped form tiles C's transpose)."""
+    tm, tn = int(info.tile_m), int(info.tile_n)
+    return (tn, tm) if info.swap_ab else (tm, tn)
 
 
 def check_sampled(p: wl.Problem, x: wl.Inputs, c_host: np.ndarray, samples: np.ndarray):

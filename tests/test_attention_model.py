@@ -93,7 +93,7 @@ def _check(Q, K, V, alpha):
     batch, Lq, _ = Q.shape
     Lk = K.shape[1]
     ref, bnd = oracle.attention(Q, K, V, batch=batch, Lq=Lq, Lk=Lk, D=D, alpha=alpha)
-    tol = oracle.attention_tolerance(ref, bnd)
+    tol = oracle.attention_tolerance(ref, bnd, Q, K, V, alpha=alpha)
     q, k, v = (oracle.decode(x, "bf16").astype(np.float32) for x in (Q, K, V))
     worst = 0.0
     for b in range(batch):

@@ -4,9 +4,11 @@ element by element against the fp64 oracle (``oracle.attention``).
 The kernel rounds the probabilities to bf16 before their product with V, as
 the two-step pair does, accumulates in fp32 and rounds O to bf16 once; the
 acceptance bound per element is ``oracle.attention_tolerance``:
-2^-7 * sum_c p_ic |V_cd| + 2^-8 * |O_id| (+1e-6).  Every operand sits inside
-a larger buffer whose padding and guards hold NaN, so a read outside Q, K or V
-turns O into NaN; O's padding holds a sentinel that must survive.
+(2^-8 + 2^-14 + eta_i) * (sum_c p_ic |V_cd| + |O_id|) + Lk * 2^-126 * max|V|,
+with eta_i the stated fp32 score allowance carried through the exponential.
+Every operand sits inside a larger buffer whose padding and guards hold NaN,
+so a read outside Q, K or V turns O into NaN; O's padding holds a sentinel
+that must survive.
 """
 from __future__ import annotations
 
@@ -93,7 +95,7 @@ def check(O, Q, K, V, alpha):
     batch, Lq, _ = Q.shape
     ref, bnd = oracle.attention(Q, K, V, batch=batch, Lq=Lq, Lk=K.shape[1], D=D, alpha=alpha)
     assert not np.isnan(O).any(), "NaN in O: a read outside Q, K or V"
-    tol = oracle.attention_tolerance(ref, bnd)
+    tol = oracle.attention_tolerance(ref, bnd, Q, K, V, alpha=alpha)
     err = np.abs(O - ref)
     bad = err > tol
     assert not bad.any(), (f"{int(bad.sum())} elements out of bound; worst at "
@@ -175,12 +177,11 @@ def test_repeat_runs_are_bitwise_identical():
     assert np.array_equal(a, b)
 
 
-def test_full_workload_sampled_rows_and_convexity():
+def test_full_workload_every_element_and_convexity():
     """batch 128, Lq = Lk = 2048, D = 128 (the attention pair's shape, with the
-    pair's inputs): sampled rows against the oracle (rows are independent, so
-    the oracle takes just those query rows), and for every row the property
-    that O is a convex combination of V's rows: min_c V_cd <= O_id <= max_c
-    V_cd, within O's final rounding."""
+    pair's inputs): every element of O against the oracle, and for every row
+    the property that O is a convex combination of V's rows:
+    min_c V_cd <= O_id <= max_c V_cd, within O's final rounding."""
     _need_gpu()
     batch, L = 128, 2048
     Q, K, V = wl.attention_qkv(batch, L, D)
@@ -188,27 +189,22 @@ def test_full_workload_sampled_rows_and_convexity():
     q = torch.from_numpy(Q.view(np.int16)).to(dev)
     k = torch.from_numpy(K.view(np.int16)).to(dev)
     v = torch.from_numpy(V.view(np.int16)).to(dev)
-    o = torch.empty_like(q)
+    o = torch.full_like(q, int(NAN16))
     desc = api.make_attn_desc(batch=batch, Lq=L, Lk=L, alpha=ALPHA)
     with api.AttnPlan(desc) as plan:
         plan.run(q, k, v, o, torch.cuda.current_stream())
         torch.cuda.synchronize()
         assert plan.device_error()[0] == api.BMM_OK
     of = o.view(torch.bfloat16).float()
-    assert not torch.isnan(of).any()
+    assert bool(torch.isfinite(of).all())
     vf = v.view(torch.bfloat16).float()
     lo, hi = vf.amin(dim=1, keepdim=True), vf.amax(dim=1, keepdim=True)
     slack = 2.0 ** -7 * torch.maximum(lo.abs(), hi.abs())
     assert bool(((of >= lo - slack) & (of <= hi + slack)).all())
     O = of.double().cpu().numpy()
-    rng = np.random.default_rng(7)
-    for b in (0, 77, 127):
-        rows = np.sort(np.concatenate([[0, 127, 128, L - 1], rng.choice(L, 28, replace=False)]))
-        rows = np.unique(rows)
-        ref, bnd = oracle.attention(np.ascontiguousarray(Q[b:b + 1, rows]), K[b:b + 1], V[b:b + 1],
-                                    batch=1, Lq=len(rows), Lk=L, D=D, alpha=ALPHA)
-        err = np.abs(O[b, rows] - ref[0])
-        assert np.all(err <= oracle.attention_tolerance(ref[0], bnd[0])), (b, float(err.max()))
+    del q, k, v, o, of, vf
+    worst = check(O, Q, K, V, ALPHA)
+    print(f"attention 128x2048x2048x128: max err/tol over all {O.size} elements = {worst:.4f}")
 
 
 def test_expired_wait_is_reported_and_the_next_run_is_clean(monkeypatch):

@@ -274,7 +274,9 @@ def _attn_run_and_check(batch, Lq, Lk, sample_items, rows, seed):
         ob = o[GUARD + b * Lq * D:GUARD + (b + 1) * Lq * D].view(Lq, D)[torch.from_numpy(rows).to(dev)]
         got = ob.view(torch.bfloat16).double().cpu().numpy()
         err = np.abs(got - ref[0])
-        tol = oracle.attention_tolerance(ref[0], bnd[0])
+        tol = oracle.attention_tolerance(ref, bnd, qb.cpu().numpy().view(np.uint16)[None],
+                                         kb.cpu().numpy().view(np.uint16), vb.cpu().numpy().view(np.uint16),
+                                         alpha=ATTN_ALPHA)[0]
         assert np.all(err <= tol), (b, float((err / tol).max()))
     del q, k, v, o
     torch.cuda.empty_cache()

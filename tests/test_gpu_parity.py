@@ -16,7 +16,7 @@ import oracle
 from dense_matmul_tensor_gb300 import bmm as api
 from dense_matmul_tensor_gb300 import workloads as wl
 
-from bmm_harness import check_full, check_sampled, run_gpu, sample_indices, decode_c
+from bmm_harness import check_full, check_sampled, decode_c, plan_tiles, run_gpu, sample_indices
 
 pytestmark = pytest.mark.gpu
 
@@ -251,13 +251,28 @@ def test_tile_configuration_does_not_change_exact_results(monkeypatch, type_c):
 
 
 # ------------------------------------------------------- full-size workloads
+#
+# Every element of C at the full sizes is compared with the fp64 oracle (the
+# oracle runs on the host cores, in slices of whole batch items), and no
+# element may be NaN or Inf.  The tile corners and seams of the plan the
+# library chose are checked once more on their own, so a failure there names
+# the seam.
+
+
+def _full_and_seams(p, x, c, info, seed, n=2000):
+    worst = check_full(p, x, c)
+    tm, tn = plan_tiles(info)
+    check_sampled(p, x, c, sample_indices(p, n, seed, tile_m=tm, tile_n=tn))
+    print(f"{p.name}: max err/tol over all {p.batch * p.M * p.N} elements = {worst:.4f}")
+    return worst
+
 
 def test_workload_gemm_4096():
     p = wl.GEMM_4096
     x = wl.make_inputs(p)
     c, info = run_gpu(p, x, guard=8192)
     assert info.tile_n == 224 and info.cta_pair == 1 and info.even_k == 1 and info.swap_ab == 0
-    check_sampled(p, x, c, sample_indices(p, 3000, 1))
+    _full_and_seams(p, x, c, info, 1)
 
 
 def test_workload_ragged():
@@ -265,7 +280,7 @@ def test_workload_ragged():
     x = wl.make_inputs(p)
     c, info = run_gpu(p, x)
     assert info.even_k == 0 and info.pack_b == 1 and info.pack_a == 0
-    check_sampled(p, x, c, sample_indices(p, 4000, 2))
+    _full_and_seams(p, x, c, info, 2)
 
 
 def test_workload_skinny():
@@ -273,20 +288,22 @@ def test_workload_skinny():
     x = wl.make_inputs(p)
     c, info = run_gpu(p, x)
     assert info.swap_ab == 1 and info.tile_n == 16
-    check_sampled(p, x, c, sample_indices(p, 4000, 3))
+    _full_and_seams(p, x, c, info, 3)
 
 
 def test_workload_attention_pair():
     """S = alpha Q K^T (fp32 out), then O = P V with P = bf16(softmax(S)) made
-    by the oracle from its own S (never from the GPU's)."""
+    by the oracle from its own S (never from the GPU's).  Both products are
+    compared with the oracle on every element."""
     qk, pv = wl.ATTN_QK, wl.ATTN_PV
     Q, Kt, V = wl.attention_qkv()
     xs = wl.Inputs(Q.ravel(), Kt.ravel(), None)
     s_host, info = run_gpu(qk, xs)
     assert info.tile_n == 256
-    check_sampled(qk, xs, s_host, sample_indices(qk, 3000, 4))
+    _full_and_seams(qk, xs, s_host, info, 4)
+    del s_host
     P = oracle.attention_probs_bf16(Q, Kt, batch=128, L=2048, D=128, alpha=qk.alpha)
     xo = wl.Inputs(P.ravel(), V.ravel(), None)
     o_host, info = run_gpu(pv, xo)
     assert info.tile_n == 128
-    check_sampled(pv, xo, o_host, sample_indices(pv, 3000, 5))
+    _full_and_seams(pv, xo, o_host, info, 5)

@@ -18,7 +18,7 @@ import torch
 from dense_matmul_tensor_gb300 import bmm as api
 from dense_matmul_tensor_gb300 import workloads as wl
 
-from bmm_harness import check_full, check_sampled, run_gpu, sample_indices
+from bmm_harness import check_full, run_gpu
 
 pytestmark = pytest.mark.gpu
 
@@ -89,7 +89,7 @@ def test_row_loader_on_the_ragged_workload(monkeypatch):
     loaded, info = run_gpu(p, x, guard=8192)
     assert info.pack_b == 2 and info.pack_a == 0
     assert np.array_equal(staged.view(np.uint8), loaded.view(np.uint8))
-    check_sampled(p, x, loaded, sample_indices(p, 2000, 7))
+    check_full(p, x, loaded)
 
 
 def test_noalloc_reads_operands_past_its_staging_area_in_place():
@@ -113,4 +113,4 @@ def test_noalloc_reads_operands_past_its_staging_area_in_place():
     assert int(err.item()) == 0
     got = C.cpu().numpy()
     assert np.array_equal(got.view(np.uint8), staged.view(np.uint8))
-    check_sampled(p, x, got, sample_indices(p, 1500, 8))
+    check_full(p, x, got)

@@ -471,3 +471,40 @@ def test_attention_oracle_matches_probs_then_product():
     two_step = Pv @ Vv
     bnd = np.abs(Pv) @ np.abs(Vv)
     assert np.all(np.abs(O - two_step) <= 2.0 ** -8 * bnd + 1e-12)   # P rounded to bf16 once
+
+
+def test_bf16_values_match_the_oracle_decode_on_all_patterns():
+    allbits = np.arange(65536, dtype=np.uint16)
+    ours = oracle.bf16_values(allbits).astype(np.float64)
+    ref = oracle.decode(allbits, "bf16")
+    fin = np.isfinite(ref)
+    assert np.array_equal(ours[fin], ref[fin])
+    assert np.array_equal(np.isnan(ours), np.isnan(ref)) and np.array_equal(np.isinf(ours), np.isinf(ref))
+
+
+def test_attention_tolerance_terms_and_what_it_admits():
+    """The fused-attention bound at alpha = 0 reduces to its fixed terms; it
+    admits the result of rounding every normalised probability and then O to
+    bf16 (the two roundings it is derived from), and it rejects an O that
+    drops one key of the softmax (a plausible kernel mistake)."""
+    batch, Lq, Lk, D = 2, 24, 96, 16
+    Q, Kt, V = _att_inputs(batch, Lq, Lk, D, 810)
+    O, bnd = oracle.attention(Q, Kt, V, batch=batch, Lq=Lq, Lk=Lk, D=D, alpha=0.0)
+    vmax = np.abs(oracle.decode(V, "bf16")).max(axis=1)
+    tol0 = oracle.attention_tolerance(O, bnd, Q, Kt, V, alpha=0.0)
+    want = (2.0 ** -8 + 2.0 ** -14) * (bnd + np.abs(O)) + Lk * 2.0 ** -126 * vmax[:, None, :]
+    assert np.array_equal(tol0, want)
+    alpha = 0.4
+    O, bnd = oracle.attention(Q, Kt, V, batch=batch, Lq=Lq, Lk=Lk, D=D, alpha=alpha)
+    tol = oracle.attention_tolerance(O, bnd, Q, Kt, V, alpha=alpha)
+    q, k, v = (oracle.decode(x, "bf16") for x in (Q, Kt, V))
+    s = alpha * np.einsum("bid,bcd->bic", q, k)
+    p = np.exp(s - s.max(axis=2, keepdims=True))
+    l = p.sum(axis=2, keepdims=True)
+    p_bf = oracle.decode(oracle.round_bf16(p), "bf16")
+    two_round = oracle.decode(oracle.round_bf16(np.einsum("bic,bcd->bid", p_bf, v) / l), "bf16")
+    assert np.all(np.abs(two_round - O) <= tol)
+    # the eta term grows with |alpha| and the norms of q and k
+    assert np.all(tol >= (2.0 ** -8 + 2.0 ** -14) * (bnd + np.abs(O)))
+    drop = np.einsum("bic,bcd->bid", p[:, :, 1:], v[:, 1:]) / p[:, :, 1:].sum(axis=2, keepdims=True)
+    assert np.any(np.abs(drop - O) > tol)

@@ -67,3 +67,41 @@ def test_noalloc_matches_bmm_run_on_two_calls_in_a_row():
         pad = np.concatenate([np.arange(b * s["sC"] + i * s["ldc"] + p.N, b * s["sC"] + (i + 1) * s["ldc"])
                               for b in range(p.batch) for i in range(p.M - 1)])
         assert np.array_equal(c_na[pad], x.C_in[pad])
+
+
+def test_noalloc_beyond_its_staging_area_reads_the_operand_in_place():
+    """A needs 84 MB of staging (lda 1027 is not a multiple of 8 elements),
+    more than the built-in 32 MiB: the call reads A in place through the
+    kernels' row loader instead.  Its output equals bmm_run's (staged) bit
+    for bit and meets the oracle's bound; the first call passes no
+    device_error pointer, the second one does."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    p = wl.Problem(batch=40, M=1024, N=256, K=1024, lda=1027, type_ab="f16", type_c="f32", seed=203)
+    desc = desc_for(p)
+    info = api.bmm_plan_query(desc)
+    assert info.pack_a == 1 and info.workspace_bytes > (32 << 20)
+    x = wl.make_inputs(p)
+    dev = torch.device("cuda:0")
+    A = torch.from_numpy(x.A.view(np.int16)).to(dev)
+    B = torch.from_numpy(x.B.view(np.int16)).to(dev)
+    nc = p.storage_elems()[2]
+    C_plan = torch.full((nc,), float("nan"), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    with api.Plan(desc) as plan:
+        plan.run(A, B, C_plan, p.alpha, p.beta, stream)
+        torch.cuda.synchronize()
+        assert plan.device_error()[0] == api.BMM_OK
+    staged = C_plan.cpu().numpy()
+    err = torch.full((1,), -1, dtype=torch.int32, device=dev)
+    for call in range(2):
+        C_na = torch.full((nc,), float("nan"), dtype=torch.float32, device=dev)
+        api.bmm_run_noalloc(desc, A, B, C_na, p.alpha, p.beta, stream,
+                            device_error=(err if call else None))
+        torch.cuda.synchronize()
+        got = C_na.cpu().numpy()
+        assert np.array_equal(got.view(np.uint8), staged.view(np.uint8)), f"call {call}"
+    assert int(err.item()) == 0
+    ref, bnd = oracle.bmm(x.A, x.B, None, **p.oracle_kwargs())
+    tol = oracle.tolerance(ref, bnd, None, alpha=p.alpha, beta=p.beta, out_bf16=False)
+    assert np.all(np.abs(decode_c(got, p) - ref) <= tol)
