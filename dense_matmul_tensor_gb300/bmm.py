@@ -44,7 +44,9 @@ class bmm_plan_info_t(ctypes.Structure):
                 ("tile_m", "tile_n", "tile_k", "stages", "swap_ab", "pack_a", "pack_b", "even_k",
                  "tmem_cols", "cta_pair")] + \
                [(n, ctypes.c_int64) for n in
-                ("tiles", "smem_bytes", "stage_bytes", "workspace_bytes")]
+                ("tiles", "smem_bytes", "stage_bytes", "workspace_bytes")] + \
+               [("stream_k", ctypes.c_int32), ("sk_tiles", ctypes.c_int32),
+                ("sk_workspace_bytes", ctypes.c_int64)]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}

@@ -45,7 +45,41 @@ struct Planned {
   uint32_t stage_bytes, a_bytes, tx_bytes, idesc, tmem_cols;
   int64_t tiles, smem_bytes, workspace_bytes;
   int32_t num_m, num_n, k_blocks, tail_steps;
+  int sk;                    // stream-K tail allowed (CTA pairs, K >= kSkMinKBlocks k-blocks)
+  int64_t sk_bytes;          // its workspace: flags, then one partial slot per CTA pair
 };
+
+// Stream-K needs enough k-blocks per tile for a piece of the tail to be worth
+// its partial's round trip through memory.
+constexpr int kSkMinKBlocks = 32;
+constexpr int64_t kSkFlagBytes = 64 * 1024;  // flags region: up to 2048 pairs x 2 CTAs x 4 warps
+
+// Workspace of the stream-K tail for `pairs` CTA pairs and tile width bn:
+// the flags, then per pair its two CTAs' 128 x bn fp32 partials.
+int64_t sk_workspace_bytes(int64_t pairs, int bn) {
+  return kSkFlagBytes + pairs * 2 * dmt::kTileM * bn * 4;
+}
+
+// DMT_BMM_STREAMK: "0" never splits, "1" splits whenever a plan allows it,
+// unset lets the planner's estimate decide.
+int stream_k_mode() {
+  const char* e = std::getenv("DMT_BMM_STREAMK");
+  if (e && e[0] == '0') return 0;
+  if (e && e[0] == '1') return 2;
+  return 1;
+}
+
+// Fewest k-blocks in a stream-K piece: kSkMinUnits, and at least half a
+// tile's, so the owner of a split tile adds at most two partials.
+int64_t sk_min_units(int64_t k_blocks) {
+  const int64_t half = (k_blocks + 1) / 2;
+  return half > dmt::kSkMinUnits ? half : dmt::kSkMinUnits;
+}
+
+// Cost of the split tail's fixup (a piece's partial written and read back,
+// and the owner's wait) in units of "one round of tile columns": measured
+// as about a quarter of a round of 256-wide tiles.
+constexpr int64_t kSkFixupCost = 64;
 
 int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 
@@ -102,7 +136,7 @@ bool row_loader_requested() {
   return e && e[0] == '1';
 }
 
-void plan(const bmm_desc_t* d, Planned* P, int sms, bool row_loader) {
+void plan(const bmm_desc_t* d, Planned* P, int sms, bool row_loader, bool allow_sk = true) {
   std::memset(P, 0, sizeof(*P));
   // Skinny M: compute C^T = op(B)^T op(A)^T so that N fills the 128-row MMA.
   P->swap = (d->M <= 64 && d->N > d->M) ? 1 : 0;
@@ -148,16 +182,41 @@ void plan(const bmm_desc_t* d, Planned* P, int sms, bool row_loader) {
   const bool pair_off = pe && pe[0] == '0';
   P->pair = (bn == 256 && P->Mv > dmt::kTileM && !pair_off) ? 1 : 0;
   const int tile_m = P->pair ? 2 * dmt::kTileM : dmt::kTileM;
-  if (bn == 256) {
+  const int64_t k_blocks = (P->K + dmt::kTileK - 1) / dmt::kTileK;
+  // Stream-K tail: with the leftover tiles split along K, the widest tile is
+  // the fastest per FLOP (a round of 256-wide pair tiles takes about as long
+  // as one of 224-wide), so no width is traded for a whole number of rounds.
+  const int sk_mode = stream_k_mode();
+  const bool sk_ok = allow_sk && P->pair && k_blocks >= kSkMinKBlocks && !row_loader && sk_mode > 0;
+  const bool large = bn == 256;
+  if (large) {
     // K-major B tiles may be any multiple of 16 rows; MN-major B tiles are
     // loaded in 64-column boxes (per CTA of a pair: BN/2 columns).
     static const int kK[3] = {256, 224, 192};
     static const int kMnSingle[2] = {256, 192};
     const int units = P->pair ? sms / 2 : sms;
+    const int64_t u = units > 0 ? units : 1;
     if (!P->b.mn_major)
-      bn = balanced_tile_n(P->batch, P->Mv, P->Nv, tile_m, units > 0 ? units : 1, kK, 3);
+      bn = balanced_tile_n(P->batch, P->Mv, P->Nv, tile_m, u, kK, 3);
     else if (!P->pair)
-      bn = balanced_tile_n(P->batch, P->Mv, P->Nv, tile_m, units > 0 ? units : 1, kMnSingle, 2);
+      bn = balanced_tile_n(P->batch, P->Mv, P->Nv, tile_m, u, kMnSingle, 2);
+    if (sk_ok) {
+      // Estimated cost in tile-column rounds: whole rounds of the balanced
+      // width, against 256-wide tiles whose leftover round is split along K
+      // (its share of a round plus the fixup; no leftover: no split).
+      const int64_t tiles_b = P->batch * ((P->Mv + tile_m - 1) / tile_m) * ((P->Nv + bn - 1) / bn);
+      const int64_t cost_b = (tiles_b + u - 1) / u * bn;
+      const int64_t tiles_s = P->batch * ((P->Mv + tile_m - 1) / tile_m) * ((P->Nv + 255) / 256);
+      const int64_t cost_s = tiles_s % u == 0 ? tiles_s / u * 256 : tiles_s * 256 / u + kSkFixupCost;
+      if (sk_mode == 2 || cost_s < cost_b) {
+        bn = 256;
+        P->sk = tiles_s % u != 0 ? 1 : 0;
+      }
+    }
+  }
+  if (large) {
+    static const int kK[3] = {256, 224, 192};
+    static const int kMnSingle[2] = {256, 192};
     // DMT_BMM_TILE_N pins one of the widths this layout allows (comparisons).
     const char* te = std::getenv("DMT_BMM_TILE_N");
     if (te && *te) {
@@ -169,6 +228,7 @@ void plan(const bmm_desc_t* d, Planned* P, int sms, bool row_loader) {
     }
   }
   P->bn = bn;
+  P->sk_bytes = P->sk ? sk_workspace_bytes(sms / 2 > 0 ? sms / 2 : 1, bn) : 0;
   const int b_rows = P->pair ? bn / 2 : bn;  // B tile rows held by one CTA
   P->a.box_rows = dmt::kTileM;
   P->b.box_rows = b_rows;
@@ -248,6 +308,13 @@ void fill_info(const Planned& P, const bmm_desc_t* d, bmm_plan_info_t* info) {
   info->smem_bytes = P.smem_bytes;
   info->stage_bytes = P.stage_bytes;
   info->workspace_bytes = P.workspace_bytes;
+  info->stream_k = P.sk;
+  if (P.sk) {
+    const int64_t pairs = kGb300Sms / 2;
+    const int64_t rem = P.tiles % pairs;
+    info->sk_tiles = static_cast<int32_t>(rem);
+    info->sk_workspace_bytes = P.sk_bytes;
+  }
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -277,12 +344,12 @@ bool prepare_kernel(int64_t smem) {
   return ok;
 }
 
-template <int BN>
+template <int BN, bool kSK = false>
 bool prepare_pair_kernel() {
   static std::once_flag once;
   static bool ok = false;
   std::call_once(once, [] {
-    ok = cudaFuncSetAttribute(dmt::bmm_tc2_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    ok = cudaFuncSetAttribute(dmt::bmm_tc2_kernel<BN, kSK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               static_cast<int>(dmt::kSmemLimit)) == cudaSuccess;
   });
   return ok;
@@ -306,6 +373,8 @@ struct bmm_plan_s {
   int sms;
   int max_pairs;  // co-resident CTA pairs for the pair kernel (0: not queried)
   void* ws;
+  void* sk_ws;        // stream-K flags and partials (P.sk_bytes; flags start at zero)
+  uint32_t sk_epoch;  // flag value of the last launch (never 0)
   uint32_t* err;
   uint64_t timeout_ns;
   int test_stall;
@@ -358,7 +427,7 @@ cudaLaunchConfig_t pair_config(int64_t pairs, int64_t smem, cudaStream_t stream,
 // Persistent grid of CTA pairs: as many as can be co-resident (queried once
 // per plan), at most one per pair tile.
 template <int BN>
-cudaError_t launch_gemm_pair(bmm_plan_s* pl, const KParams& kp, cudaStream_t stream) {
+cudaError_t launch_gemm_pair(bmm_plan_s* pl, KParams kp, cudaStream_t stream) {
   if (!prepare_pair_kernel<BN>()) return cudaErrorInvalidValue;
   cudaLaunchAttribute attr[1];
   if (pl->max_pairs == 0) {
@@ -368,7 +437,35 @@ cudaError_t launch_gemm_pair(bmm_plan_s* pl, const KParams& kp, cudaStream_t str
     if (e != cudaSuccess) return e;
     pl->max_pairs = n > 0 ? n : 1;
   }
-  const int64_t pairs = pl->P.tiles < pl->max_pairs ? pl->P.tiles : pl->max_pairs;
+  int64_t pairs = pl->P.tiles < pl->max_pairs ? pl->P.tiles : pl->max_pairs;
+  // Stream-K tail: whole rounds over all resident pairs, then the leftover
+  // tiles' k-blocks in equal ranges (at least kSkMinUnits each) over as many
+  // pairs as that allows.
+  const int64_t G = pl->max_pairs;
+  if (BN == 256 && pl->P.sk && pl->sk_ws && G <= kSkFlagBytes / 32 &&
+      sk_workspace_bytes(G, BN) <= pl->P.sk_bytes) {
+    const int64_t waves = pl->P.tiles / G, rem = pl->P.tiles % G;
+    if (rem > 0) {
+      const int64_t units = rem * pl->P.k_blocks;
+      int64_t skp = units / sk_min_units(pl->P.k_blocks);
+      skp = skp < 1 ? 1 : (skp > G ? G : skp);
+      if (++pl->sk_epoch == 0) pl->sk_epoch = 1;
+      kp.sk_tiles = static_cast<int32_t>(rem);
+      kp.sk_pairs = static_cast<int32_t>(skp);
+      kp.sk_first = waves * G;
+      kp.sk_epoch = pl->sk_epoch;
+      kp.sk_flags = static_cast<uint32_t*>(pl->sk_ws);
+      kp.sk_ws = reinterpret_cast<float4*>(static_cast<char*>(pl->sk_ws) + kSkFlagBytes);
+      pairs = waves > 0 ? G : skp;
+    }
+  }
+  if constexpr (BN == 256) {
+    if (kp.sk_tiles > 0) {
+      if (!prepare_pair_kernel<BN, true>()) return cudaErrorInvalidValue;
+      cudaLaunchConfig_t cfg = pair_config(pairs, pl->P.smem_bytes, stream, attr, block_threads(kp));
+      return cudaLaunchKernelEx(&cfg, dmt::bmm_tc2_kernel<BN, true>, kp, pl->map[0], pl->map[1], pl->map[2]);
+    }
+  }
   cudaLaunchConfig_t cfg = pair_config(pairs, pl->P.smem_bytes, stream, attr, block_threads(kp));
   return cudaLaunchKernelEx(&cfg, dmt::bmm_tc2_kernel<BN>, kp, pl->map[0], pl->map[1], pl->map[2]);
 }
@@ -468,6 +565,15 @@ bmm_status_t bmm_create(const bmm_desc_t* desc, bmm_plan_t* out) {
   }
   if (pl->P.workspace_bytes > 0 &&
       cudaMalloc(&pl->ws, static_cast<size_t>(pl->P.workspace_bytes)) != cudaSuccess) {
+    cudaFree(pl->err);
+    delete pl;
+    return BMM_ERR_CUDA;
+  }
+  if (pl->P.sk_bytes > 0 &&
+      (cudaMalloc(&pl->sk_ws, static_cast<size_t>(pl->P.sk_bytes)) != cudaSuccess ||
+       cudaMemset(pl->sk_ws, 0, static_cast<size_t>(kSkFlagBytes)) != cudaSuccess)) {
+    cudaFree(pl->sk_ws);
+    cudaFree(pl->ws);
     cudaFree(pl->err);
     delete pl;
     return BMM_ERR_CUDA;
@@ -619,6 +725,7 @@ bmm_status_t bmm_destroy(bmm_plan_t pl) {
   if (!pl) return BMM_OK;
   bmm_status_t st = BMM_OK;
   if (pl->ws && cudaFree(pl->ws) != cudaSuccess) st = BMM_ERR_CUDA;
+  if (pl->sk_ws && cudaFree(pl->sk_ws) != cudaSuccess) st = BMM_ERR_CUDA;
   if (pl->err && cudaFree(pl->err) != cudaSuccess) st = BMM_ERR_CUDA;
   delete pl;
   return st;
@@ -716,9 +823,10 @@ extern "C" bmm_status_t bmm_run_noalloc(const bmm_desc_t* desc, const void* A, c
   bmm_plan_s pl;  // on the stack: nothing is allocated for the call
   std::memset(static_cast<void*>(&pl), 0, sizeof(pl));
   pl.d = *desc;
-  plan(desc, &pl.P, sms, row_loader_requested());
+  // no stream-K tail here: its partials would need more scratch than the array holds
+  plan(desc, &pl.P, sms, row_loader_requested(), false);
   // staging larger than the built-in scratch: the row loader reads those operands
-  if (pl.P.workspace_bytes > static_cast<int64_t>(kNoAllocStagingMax)) plan(desc, &pl.P, sms, true);
+  if (pl.P.workspace_bytes > static_cast<int64_t>(kNoAllocStagingMax)) plan(desc, &pl.P, sms, true, false);
   unsigned char* scratch = nullptr;
   const bmm_status_t sst = noalloc_scratch(dev, &scratch);
   if (sst != BMM_OK) return sst;

@@ -76,7 +76,13 @@ enum WaitSite : uint32_t {
   kSiteEpiAccFull = 4,
   kSiteTestStall = 5,
   kSiteSchedule = 6,
+  kSiteStreamK = 7,
 };
+
+// Stream-K tail of the CTA-pair kernel: a piece of k-blocks [ka, kb) of one
+// tile has at least this many k-blocks, and at least half the tile's (so a
+// tile has at most three pieces and its owner adds at most two partials).
+constexpr int kSkMinUnits = 8;
 
 // One problem of a grouped launch: an entry of a device table built by the
 // host (tensor maps first, so each is 128-byte aligned).  tile_begin is the
@@ -127,7 +133,79 @@ struct KParams {
   int32_t ngroups;
   int32_t ldg_mask;        // bit 0: A, bit 1: B read by the row loader (tx_bytes excludes them)
   LdgOperand ldg[2];       // A, B
+  // Stream-K tail (CTA-pair kernel; sk_tiles == 0: off).  The first
+  // sk_first tiles run whole, round-robin over the pairs; the
+  // k-blocks of the last sk_tiles tiles are cut into sk_pairs equal ranges,
+  // one per pair.  A piece without k-block 0 leaves its fp32 partial in
+  // sk_ws and raises its flags to sk_epoch; the piece with k-block 0 adds the
+  // other pieces' partials and writes C.
+  int32_t sk_tiles, sk_pairs;
+  int64_t sk_first;        // first tile of the tail (whole rounds x pairs)
+  uint32_t sk_epoch;       // this launch's flag value (never 0)
+  float4* sk_ws;           // [pair][rank][quarter][chunk][8][32 rows] float4
+  uint32_t* sk_flags;      // [pair][rank][quarter]
 };
+
+// A stream-K piece: k-blocks [ka, kb) of tile `tile`.  kind 0: the whole
+// tile (a range that happens to cover it); kind 1: no k-block 0 (its partial
+// goes to the workspace slot of its pair); kind 2: the piece with k-block 0
+// of a split tile, which adds the partials of pairs [q_lo, q_hi) and writes C.
+struct SkPiece {
+  int64_t tile;
+  int32_t ka, kb, kind, q_lo, q_hi;
+};
+
+// Piece si (0 or 1) of pair `pair`: the pair's range of the tail's
+// sk_tiles * k_blocks k-blocks, cut at tile boundaries (a range is at most
+// one tile long, so it has at most two pieces).  False: no such piece.
+__device__ __forceinline__ bool sk_piece(const KParams& p, int64_t pair, int si, SkPiece& it) {
+  if (!p.sk_tiles || pair >= p.sk_pairs) return false;
+  const int64_t KB = p.k_blocks;
+  const int64_t U = static_cast<int64_t>(p.sk_tiles) * KB;
+  const int64_t G = p.sk_pairs;
+  const int64_t u0 = pair * U / G, u1 = (pair + 1) * U / G;
+  if (u1 <= u0) return false;
+  const int64_t t0 = u0 / KB;  // tile of the first piece, within the tail
+  int64_t tt, s, e;
+  if (si == 0) {
+    tt = t0;
+    s = u0;
+    e = (t0 + 1) * KB < u1 ? (t0 + 1) * KB : u1;
+  } else if (u1 > (t0 + 1) * KB) {
+    tt = t0 + 1;
+    s = tt * KB;
+    e = u1;
+  } else {
+    return false;
+  }
+  it.tile = p.sk_first + tt;
+  it.ka = static_cast<int32_t>(s - tt * KB);
+  it.kb = static_cast<int32_t>(e - tt * KB);
+  it.q_lo = it.q_hi = 0;
+  if (it.ka > 0) {
+    it.kind = 1;
+  } else if (it.kb == KB) {
+    it.kind = 0;
+  } else {
+    // the rest of the tile belongs to the next pairs, each in its first piece
+    it.kind = 2;
+    it.q_lo = static_cast<int32_t>(pair + 1);
+    int64_t q = pair + 1;
+    while (q < G && q * U / G < (tt + 1) * KB) ++q;
+    it.q_hi = static_cast<int32_t>(q);
+  }
+  return true;
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* ptr) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release_gpu(uint32_t* ptr, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(ptr), "r"(v) : "memory");
+}
 
 // What the epilogue needs about C, for the launch or for one grouped problem.
 struct EpiArgs {
@@ -977,6 +1055,117 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem_base, p.tmem_cols);
 }
 
+// Stream-K fixup of one epilogue warp's 32 accumulator rows (the piece with a
+// split tile's first k-block): adds the partials that pairs [q_lo, q_hi)
+// left in their workspace slots to the accumulator in Tensor Memory (columns
+// taddr .. taddr + BN - 1), after which the epilogue reads it as a whole
+// tile.  Chunk c of pair x's partial is 4 KB at p.sk_ws + (slot(x) + c) * 256
+// float4.  The operand ring is idle when this runs (this piece is its pair's
+// last item and all its MMAs are complete), so the partials come in by bulk
+// copies into `region` (this warp's quarter of the ring: an mbarrier, then
+// 4 KB buffers), as many chunks per batch as the buffers hold.
+template <int BN>
+__device__ __forceinline__ bool sk_fixup(const KParams& p, uint8_t* region, uint32_t region_addr,
+                                      uint32_t region_bytes, int64_t slot_base_stride, int64_t slot_off,
+                                      int q_lo, int q_hi, uint32_t taddr, int lane, Abort ab) {
+  const int n = q_hi - q_lo;
+  // the contributors' flags: partial written (bounded wait, acquire)
+  for (int x = q_lo; x < q_hi; ++x) {
+    const uint32_t* f = p.sk_flags + (x * slot_base_stride + slot_off) / (BN / 32);
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t spin = 0;; ++spin) {
+      if (__all_sync(0xffffffffu, ld_acquire_gpu(f) == p.sk_epoch)) break;
+      if ((spin & 15u) == 15u) {
+        int bad = 0;
+        if (lane == 0) bad = *ab.flag ? 1 : (global_timer_ns() - t0 > ab.timeout_ns ? 2 : 0);
+        bad = __shfl_sync(0xffffffffu, bad, 0);
+        if (bad) {
+          if (bad == 2 && lane == 0) {
+            *ab.flag = 1u;
+            atomicCAS(ab.err, 0u, kErrTag | (kSiteStreamK << 8) | (blockIdx.x & 0xFFu));
+          }
+          return false;
+        }
+      }
+    }
+  }
+  const uint32_t bar = region_addr;
+  const uint32_t nbuf = (region_bytes - 128u) / 4096u;
+  const int per_batch = static_cast<int>(nbuf) / n;  // chunks per batch (n <= 2: at least 5)
+  if (lane == 0) {
+    mbar_init(bar, 1);
+    fence_barrier_init();
+  }
+  __syncwarp();
+  uint32_t phase = 0;
+  for (int c0 = 0; c0 < BN / 32; c0 += per_batch) {
+    const int c1 = c0 + per_batch < BN / 32 ? c0 + per_batch : BN / 32;
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bar, static_cast<uint32_t>((c1 - c0) * n) * 4096u);
+      for (int c = c0; c < c1; ++c)
+        for (int x = q_lo; x < q_hi; ++x)
+          bulk_load(region_addr + 128u + static_cast<uint32_t>((c - c0) * n + (x - q_lo)) * 4096u,
+                    p.sk_ws + (x * slot_base_stride + slot_off + c) * 256, 4096u, bar);
+    }
+    if (!warp_wait_bounded(bar, phase, ab, kSiteStreamK, lane)) return false;
+    phase ^= 1u;
+    for (int c = c0; c < c1; ++c) {
+      float v[32];
+      tmem_ld_32cols(taddr + 32u * c, v);
+      tmem_wait_ld();
+      for (int x = 0; x < n; ++x) {
+        const float4* src = reinterpret_cast<const float4*>(region + 128u + ((c - c0) * n + x) * 4096u) + lane;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float4 s4 = src[j * 32];
+          v[4 * j] += s4.x;
+          v[4 * j + 1] += s4.y;
+          v[4 * j + 2] += s4.z;
+          v[4 * j + 3] += s4.w;
+        }
+      }
+      tmem_st_32cols(taddr + 32u * c, v);
+    }
+    tmem_wait_st();
+    // the next batch's copies (async proxy) overwrite what was just read
+    fence_proxy_async_shared();
+    __syncwarp();
+  }
+  // consumed: clear the flags for the next launch
+  if (lane == 0)
+    for (int x = q_lo; x < q_hi; ++x) p.sk_flags[(x * slot_base_stride + slot_off) / (BN / 32)] = 0u;
+  tc_fence_before_sync();
+  return true;
+}
+
+// Stream-K piece without its tile's first k-block (kind 1): this warp's 32
+// accumulator rows go to its workspace slot `dst` instead of C (rows as
+// lanes, 8 float4 per row, so each float4 index is a contiguous 512-byte run
+// across the warp), the accumulator is released to the leader (`acce`), and
+// once every lane's stores are visible the flag is raised to this launch's
+// epoch (release).
+template <int BN>
+__device__ __forceinline__ void sk_keep_partial(const KParams& p, float4* dst, uint32_t* flag, uint32_t taddr,
+                                             uint32_t acce, int lane) {
+#pragma unroll 1
+  for (int c = 0; c < BN / 32; ++c) {
+    float v[32];
+    tmem_ld_32cols(taddr + 32u * c, v);
+    tmem_wait_ld();
+    if (c == BN / 32 - 1) {
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(acce);
+    }
+    float4* d = dst + c * 256 + lane;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) d[j * 32] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+  }
+  __threadfence();
+  __syncwarp();
+  if (lane == 0) st_release_gpu(flag, p.sk_epoch);
+}
+
 // bmm_tc2_kernel: the same pipeline over CTA pairs (a cluster of 2).  The
 // pair computes a 256 x BN tile with tcgen05.mma.cta_group::2: CTA r holds
 // rows [128r, 128r+128) of the A tile and rows [r*BN/2, (r+1)*BN/2) of the
@@ -993,7 +1182,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 //     empty" barrier (8 arrivals per phase).
 //   - A cluster barrier at the end keeps either CTA from exiting (or freeing
 //     Tensor Memory) while the other can still signal it.
-template <int BN>
+//   - kSK (stream-K tail, p.sk_tiles > 0): after its whole tiles each pair
+//     runs at most two pieces (sk_piece); see sk_keep_partial and sk_fixup.
+//     A separate instantiation, so launches without a split run code with
+//     none of it.
+template <int BN, bool kSK = false>
 __global__ void __launch_bounds__(kThreads, 1)
     bmm_tc2_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmC) {
@@ -1022,6 +1215,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t rank = cluster_ctarank();
   const bool leader = rank == 0;
   const int64_t pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+  // whole tiles, round-robin over the pairs; then (stream-K) at most two pieces
+  const int64_t dp_end = kSK ? p.sk_first : p.tiles;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -1060,7 +1255,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // kLdg: some operand comes from the row loaders (its TMA loads are
       // skipped, and the leader may have no bytes to expect).  A separate copy
       // of the loop keeps the TMA-only issue sequence as it is.
-      auto produce = [&](auto has_ldg) {
+      auto produce_dp = [&](auto has_ldg) {
         constexpr bool kLdg = decltype(has_ldg)::value;
         for (int64_t t = pair; t < p.tiles && ok; t += npairs) {
           int b, mb, nb;
@@ -1106,8 +1301,65 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       };
-      if (p.ldg_mask) produce(BoolC<true>{});
-      else produce(BoolC<false>{});
+      auto produce = [&](auto has_ldg) {
+        constexpr bool kLdg = decltype(has_ldg)::value;
+        // k-blocks [k_lo, k_hi) of tile t
+        auto load_tile = [&](int64_t t, int k_lo, int k_hi) {
+          int b, mb, nb;
+          decode_tile(t, p, b, mb, nb);
+          const int m_own = mb * (2 * kTileM) + static_cast<int>(rank) * kTileM;
+          const int n_own = nb * BN + static_cast<int>(rank) * BNH;
+          const int za = p.a_bcast ? 0 : b, zb = p.b_bcast ? 0 : b;
+          for (int kb = k_lo; kb < k_hi; ++kb, ++it) {
+            const uint32_t s = it % S, ph = (it / S) & 1u;
+            if (!wait_bounded<true>(empty_bar(s), ph ^ 1u, ab, kSiteProducerEmpty)) {
+              ok = false;
+              break;
+            }
+            const uint32_t a_dst = sbase + s * p.stage_bytes;
+            const uint32_t b_dst = a_dst + p.a_bytes;
+            if constexpr (kLdg) {
+              if (leader) {
+                if (p.tx_bytes) mbar_arrive_expect_tx(full_bar(s), 2u * p.tx_bytes);
+                else mbar_arrive(full_bar(s));  // both operands come from the row loaders
+              }
+            } else {
+              if (leader) mbar_arrive_expect_tx(full_bar(s), 2u * p.tx_bytes);
+            }
+            const uint32_t fb = mapa_shared(full_bar(s), 0);  // the leader's barrier
+            const int k0 = kb * kTileK;
+            if (!kLdg || !(p.ldg_mask & 1)) {
+              if (!p.a_mn) {
+                tma_load_3d_pair(a_dst, &tmA, fb, k0, m_own, za);
+              } else {
+                tma_load_3d_pair(a_dst, &tmA, fb, m_own, k0, za);
+                tma_load_3d_pair(a_dst + 8192u, &tmA, fb, m_own + 64, k0, za);
+              }
+            }
+            if (!kLdg || !(p.ldg_mask & 2)) {
+              if (!p.b_mn) {
+                tma_load_3d_pair(b_dst, &tmB, fb, k0, n_own, zb);
+              } else {
+#pragma unroll
+                for (int h = 0; h < BNH / 64; ++h)
+                  tma_load_3d_pair(b_dst + 8192u * h, &tmB, fb, n_own + 64 * h, k0, zb);
+              }
+            }
+          }
+        };
+        for (int64_t t = pair; t < dp_end && ok; t += npairs) load_tile(t, 0, p.k_blocks);
+        if constexpr (kSK) {
+          SkPiece pc;
+          for (int si = 0; si < 2 && ok && sk_piece(p, pair, si, pc); ++si) load_tile(pc.tile, pc.ka, pc.kb);
+        }
+      };
+      if constexpr (!kSK) {
+        if (p.ldg_mask) produce_dp(BoolC<true>{});
+        else produce_dp(BoolC<false>{});
+      } else {
+        if (p.ldg_mask) produce(BoolC<true>{});
+        else produce(BoolC<false>{});
+      }
       // The leader's full barriers count both CTAs' bytes: once the last S
       // have completed, no load of either CTA is still in flight.
       if (leader) {
@@ -1128,7 +1380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // kClusterAcq: the peer's row loader writes its stage with plain stores,
       // so the full waits take its release at cluster scope (a separate copy
       // of the loop keeps the TMA-only path's issue loop as it is)
-      auto mma_tiles = [&](auto cluster_acq) {
+      auto mma_dp = [&](auto cluster_acq) {
         constexpr bool kClusterAcq = decltype(cluster_acq)::value;
         for (int64_t t = pair; t < p.tiles && ok; t += npairs, ++tl) {
           const uint32_t acc = tl & 1u, aph = (tl >> 1) & 1u;
@@ -1158,8 +1410,49 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_commit_pair_multicast(accf_bar(acc), 0x3);  // accumulator halves complete
         }
       };
-      if (p.ldg_mask) mma_tiles(BoolC<true>{});
-      else mma_tiles(BoolC<false>{});
+      auto mma_tiles = [&](auto cluster_acq) {
+        constexpr bool kClusterAcq = decltype(cluster_acq)::value;
+        // k-blocks [k_lo, k_hi) of the next tile into accumulator tl & 1
+        auto mma_tile = [&](int k_lo, int k_hi) {
+          const uint32_t acc = tl & 1u, aph = (tl >> 1) & 1u;
+          if (!wait_bounded<true>(acce_bar(acc), aph ^ 1u, ab, kSiteMmaAccEmpty)) {
+            ok = false;
+            return;
+          }
+          tc_fence_after_sync();
+          const uint32_t d_tmem = tmem_base + acc * BN;
+          for (int kb = k_lo; kb < k_hi; ++kb) {
+            if (!(kClusterAcq ? wait_bounded_cluster(full_bar(s), ph, ab, kSiteMmaFull)
+                              : wait_bounded<true>(full_bar(s), ph, ab, kSiteMmaFull))) {
+              ok = false;
+              break;
+            }
+            // No tcgen05 fence here (see the single-CTA kernel).
+            const int nsteps = (kb == p.k_blocks - 1) ? p.tail_steps : kTileK / kUmmaK;
+            issue_kblock<true>(d_tmem, alo0 + s * sstep, blo0 + s * sstep, hi, hi, astep, bstep,
+                               p.idesc, nsteps, kb == k_lo);
+            tc_commit_pair_multicast(empty_bar(s), 0x3);  // slot free in both CTAs
+            if (++s == static_cast<uint32_t>(S)) {
+              s = 0;
+              ph ^= 1u;
+            }
+          }
+          if (!ok) return;
+          tc_commit_pair_multicast(accf_bar(acc), 0x3);  // accumulator halves complete
+        };
+        for (int64_t t = pair; t < dp_end && ok; t += npairs, ++tl) mma_tile(0, p.k_blocks);
+        if constexpr (kSK) {
+          SkPiece pc;
+          for (int si = 0; si < 2 && ok && sk_piece(p, pair, si, pc); ++si, ++tl) mma_tile(pc.ka, pc.kb);
+        }
+      };
+      if constexpr (!kSK) {
+        if (p.ldg_mask) mma_dp(BoolC<true>{});
+        else mma_dp(BoolC<false>{});
+      } else {
+        if (p.ldg_mask) mma_tiles(BoolC<true>{});
+        else mma_tiles(BoolC<false>{});
+      }
       tc_commit_pair(drain_bar);
       drain_wait(drain_bar, 0u);
     }
@@ -1176,21 +1469,57 @@ __global__ void __launch_bounds__(kThreads, 1)
     const EpiArgs ea = epi_args(p);
     // row-major C with beta != 0 on the direct path: C_in two chunks deep
     const bool pre = p.beta != 0.0f && !p.c_tma && !p.c_trans;
-    for (int64_t t = pair; t < p.tiles; t += npairs, ++tl) {
+    // Whole tiles first (round-robin), then at most two stream-K pieces: a
+    // piece without its tile's first k-block keeps its partial, the piece
+    // with it adds the others' partials before storing the tile as usual.
+    int64_t t_next = pair;
+    int si = 0;
+    for (;; ++tl) {
+      int64_t t;
+      int kind = 0;
+      SkPiece pc;
+      if (t_next < dp_end) {
+        t = t_next;
+        t_next += npairs;
+      } else if (kSK && si < 2 && sk_piece(p, pair, si, pc)) {
+        ++si;
+        t = pc.tile;
+        kind = pc.kind;
+      } else {
+        break;
+      }
       const uint32_t acc = tl & 1u, aph = (tl >> 1) & 1u;
       int b, mb, nb;
       decode_tile(t, p, b, mb, nb);
       const int row0 = mb * (2 * kTileM) + static_cast<int>(rank) * kTileM + q * 32;
       const int64_t cbase = static_cast<int64_t>(b) * p.sC;
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
       float cin[32];
-      if (pre) prefetch_cin(ea, cin, lane, row0, nb * BN, cbase);
-      int ok = 1;
-      if (lane == 0) ok = wait_bounded(accf_bar(acc), aph, ab, kSiteEpiAccFull) ? 1 : 0;
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
+      if (pre && kind == 0) prefetch_cin(ea, cin, lane, row0, nb * BN, cbase);
+      // the epilogue waits a whole mainloop: lane 0 parks (no spinning that
+      // would take issue slots from the producer and MMA threads)
+      int okw = 1;
+      if (lane == 0) okw = wait_bounded(accf_bar(acc), aph, ab, kSiteEpiAccFull) ? 1 : 0;
+      okw = __shfl_sync(0xffffffffu, okw, 0);
+      if (!okw) break;
       __syncwarp();
       tc_fence_after_sync();
-      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+      constexpr int64_t slot_stride = 2 * 4 * (BN / 32);  // float4 blocks of 4 KB per pair
+      if (kSK && kind == 1) {
+        const int64_t slot_off = (rank * 4 + q) * (BN / 32);
+        sk_keep_partial<BN>(p, p.sk_ws + (pair * slot_stride + slot_off) * 256,
+                            p.sk_flags + (pair * 2 + rank) * 4 + q, taddr,
+                            acc ? acce_leader1 : acce_leader0, lane);
+        continue;
+      }
+      if (kSK && kind == 2) {
+        const int64_t slot_off = (rank * 4 + q) * (BN / 32);
+        const uint32_t quarter_bytes = ring_bytes / 4u;
+        if (!sk_fixup<BN>(p, smem + (warp - 2) * quarter_bytes, sbase + (warp - 2) * quarter_bytes,
+                          quarter_bytes, slot_stride, slot_off, pc.q_lo, pc.q_hi, taddr, lane, ab))
+          break;
+        if (pre) prefetch_cin(ea, cin, lane, row0, nb * BN, cbase);
+      }
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
         float v[32];
@@ -1205,8 +1534,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           // skipped outright when wholly outside C (see the single-CTA kernel)
           if (row0 < p.Mv && nb * BN + 32 * c < p.Nv) {
             const uint32_t k = nbox++ & 1u;
-            store_chunk_tma(epi_args(p), &tmC, v, boxes + k * kEpiBoxBytes,
-                            boxes_addr + k * kEpiBoxBytes, lane, row0, nb * BN + 32 * c, b);
+            store_chunk_tma(ea, &tmC, v, boxes + k * kEpiBoxBytes, boxes_addr + k * kEpiBoxBytes, lane,
+                            row0, nb * BN + 32 * c, b);
           }
         } else if (pre) {
           float nxt[32];

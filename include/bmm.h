@@ -103,7 +103,13 @@ typedef struct {
   int64_t tiles;                  /* output tiles over the whole batch */
   int64_t smem_bytes;             /* dynamic shared memory per CTA */
   int64_t stage_bytes;            /* bytes of one CTA's ring stage (its A and B tile parts) */
-  int64_t workspace_bytes;        /* device workspace the plan owns */
+  int64_t workspace_bytes;        /* device workspace for staged operands */
+  int32_t stream_k;               /* 1: the tiles left over after the last whole round
+                                     are split along K over the CTA pairs (see bmm_run) */
+  int32_t sk_tiles;               /* tiles split that way when all of the device's CTA
+                                     pairs are resident (0: none) */
+  int64_t sk_workspace_bytes;     /* device memory the plan keeps for the split's fp32
+                                     partial sums and flags */
 } bmm_plan_info_t;
 
 typedef struct bmm_plan_s* bmm_plan_t;
@@ -151,6 +157,23 @@ BMM_API bmm_status_t bmm_get_plan_info(bmm_plan_t plan, bmm_plan_info_t* info);
  * alignment, as does C.  Returns BMM_OK once the work is enqueued,
  * BMM_ERR_INVALID_ARG (null plan or pointer), or BMM_ERR_CUDA (launch
  * failure).  Does not synchronise.
+ *
+ * Stream-K tail (plans with cta_pair = 1, K >= 2048 and no operand read by
+ * the row loader; stream_k in bmm_plan_info_t): the CTA pairs first run
+ * whole 256 x 256 tiles in rounds; the tiles left over after the last whole
+ * round ("Triton Optimization Reference", section 7: the last wave of a
+ * persistent grid) are cut along K into equal ranges of k-blocks, one per
+ * pair, so every pair finishes at about the same time.  A range covers the
+ * end of one tile and the start of the next; the piece of a tile without its
+ * first k-block leaves its fp32 partial sum in the plan's stream-K workspace
+ * and raises a flag, and the piece with the first k-block waits for those
+ * flags, adds the partials and writes C.  The sum is still accumulated in
+ * fp32 (only its order changes).  Every pair of the launch must be resident
+ * at once: with other kernels holding SMs concurrently, a wait for a flag can
+ * run out, which is reported as BMM_ERR_DEVICE_TIMEOUT.  The environment
+ * variable DMT_BMM_STREAMK=0 at plan time turns the split off.  A plan whose
+ * launch was cut short by a device error should be destroyed: its flags may
+ * be left raised.
  */
 BMM_API bmm_status_t bmm_run(bmm_plan_t plan, const void* A, const void* B, void* C,
                      float alpha, float beta, void* stream);

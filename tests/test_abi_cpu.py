@@ -183,6 +183,31 @@ def test_wave_balanced_tile_width(lib, monkeypatch):
     assert api.bmm_plan_query(desc_for(wl.RAGGED)).tile_n == 256
 
 
+def test_stream_k_tail_choice(lib, monkeypatch):
+    # 8192^3 on 76 pairs: 1024 tiles of 256 x 256 = 13 whole rounds + 36 tiles;
+    # splitting those along K beats the best whole-round width (256: 14 rounds)
+    d = _desc(batch=1, M=8192, N=8192, K=8192, lda=8192, ldb=8192, ldc=8192, strideA=8192 * 8192,
+              strideB=8192 * 8192, strideC=8192 * 8192, transB=1, typeC="bf16")
+    info = api.bmm_plan_query(d)
+    assert info.stream_k == 1 and info.tile_n == 256 and info.cta_pair == 1
+    assert info.tiles == 1024 and info.sk_tiles == 1024 - 13 * 76
+    assert info.sk_workspace_bytes >= 76 * 2 * 128 * 256 * 4
+    # 4096^3: four whole rounds of 256 x 224 tiles cost less than 3.37 rounds
+    # of 256 x 256 plus the split's fixup, so no split
+    g = api.bmm_plan_query(desc_for(wl.GEMM_4096))
+    assert g.stream_k == 0 and g.sk_tiles == 0 and g.sk_workspace_bytes == 0 and g.tile_n == 224
+    # forced on where allowed, off everywhere
+    monkeypatch.setenv("DMT_BMM_STREAMK", "1")
+    f = api.bmm_plan_query(desc_for(wl.GEMM_4096))
+    assert f.stream_k == 1 and f.tile_n == 256 and f.sk_tiles == 256 - 3 * 76
+    # short K (fewer than 32 k-blocks) and single-CTA tiles never split
+    assert api.bmm_plan_query(desc_for(wl.RAGGED)).stream_k == 0
+    assert api.bmm_plan_query(desc_for(wl.ATTN_QK)).stream_k == 0
+    assert api.bmm_plan_query(desc_for(wl.SKINNY)).stream_k == 0
+    monkeypatch.setenv("DMT_BMM_STREAMK", "0")
+    assert api.bmm_plan_query(d).stream_k == 0
+
+
 def test_grouped_create_validates_before_any_device_call(lib):
     ok = dict(M=64, N=64, K=64, lda=64, ldb=64, ldc=64)
     for bad, code in [(dict(M=-1), api.BMM_ERR_INVALID_ARG), (dict(lda=10), api.BMM_ERR_INVALID_ARG),
