@@ -60,17 +60,17 @@ RECIPE_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustai
 # keyed by a hash of that kernel's sources and the workload: reported only
 # while those sources are unchanged.
 NCU_TRAFFIC = {
-    ("103267ee80d86de8", "gemm_4096x4096x4096_tn_bf16"): 85869056 + 17398016,
+    ("2fb28f8081b39449", "gemm_4096x4096x4096_tn_bf16"): 86033152 + 17498112,
     # captured at batch 64 and scaled by 2 to the batch-128 launch (every query
     # tile does the same work); most of O's write-back happens after the kernel
-    ("499122a6c61be6ec", "attn_fused_b128_2048x2048x128_bf16"): 2 * (100737536 + 5867776),
+    ("4b82bb8108cce335", "attn_fused_b128_2048x2048x128_bf16"): 2 * (100736256 + 6720512),
 }
 # Tensor-pipe activity of the same captures (sm__pipe_tensor_cycles_active,
 # % of elapsed cycles): the hardware's own measure of how busy the tensor
 # cores were, reported beside the fraction of the measured cuBLAS peak.
 NCU_TENSOR_ACTIVE_PCT = {
-    ("103267ee80d86de8", "gemm_4096x4096x4096_tn_bf16"): 71.82,
-    ("499122a6c61be6ec", "attn_fused_b128_2048x2048x128_bf16"): 40.81,
+    ("2fb28f8081b39449", "gemm_4096x4096x4096_tn_bf16"): 71.56,
+    ("4b82bb8108cce335", "attn_fused_b128_2048x2048x128_bf16"): 40.73,
 }
 
 # the sources each kernel family is built from

@@ -46,7 +46,8 @@ class bmm_plan_info_t(ctypes.Structure):
                [(n, ctypes.c_int64) for n in
                 ("tiles", "smem_bytes", "stage_bytes", "workspace_bytes")] + \
                [("stream_k", ctypes.c_int32), ("sk_tiles", ctypes.c_int32),
-                ("sk_workspace_bytes", ctypes.c_int64)]
+                ("sk_workspace_bytes", ctypes.c_int64),
+                ("stages_bf16_box", ctypes.c_int32), ("reserved0", ctypes.c_int32)]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}

@@ -42,6 +42,7 @@ struct Planned {
   int64_t batch, Mv, Nv, K;
   Operand a, b;
   int bn, stages;
+  int stages_bf16_box;       // CTA pairs: ring depth of launches whose C goes out as bf16 box stores
   uint32_t stage_bytes, a_bytes, tx_bytes, idesc, tmem_cols;
   int64_t tiles, smem_bytes, workspace_bytes;
   int32_t num_m, num_n, k_blocks, tail_steps;
@@ -76,10 +77,43 @@ int64_t sk_min_units(int64_t k_blocks) {
   return half > dmt::kSkMinUnits ? half : dmt::kSkMinUnits;
 }
 
+// Two-way split: the contributor's k-blocks.  Its partial reaches the
+// workspace about kSkPublishKBlocks k-block times after its accumulator (the
+// owner's side then costs little more than the usual epilogue), so the
+// owner takes that many more k-blocks than the contributor.
+// DMT_BMM_SK_PUBLISH_KB overrides the constant (comparisons).
+constexpr int64_t kSkPublishKBlocks = 16;
+
+int64_t sk_publish_kblocks() {
+  const char* e = std::getenv("DMT_BMM_SK_PUBLISH_KB");
+  if (e && *e) {
+    const long v = std::atol(e);
+    if (v >= 0 && v < 4096) return v;
+  }
+  return kSkPublishKBlocks;
+}
+
+int64_t sk_contributor_kblocks(int64_t k_blocks) {
+  const int64_t c = (k_blocks - sk_publish_kblocks()) / 2;
+  return c < 1 ? 1 : (c > k_blocks / 2 ? k_blocks / 2 : c);
+}
+
 // Cost of the split tail's fixup (a piece's partial written and read back,
 // and the owner's wait) in units of "one round of tile columns": measured
 // as about a quarter of a round of 256-wide tiles.
 constexpr int64_t kSkFixupCost = 64;
+
+// ... and of the two-way split's: the owner's copy of the partial and its
+// add in the epilogue, and 256-wide rounds against the balanced width's
+// (measured on 4096^3: the split ends with 224-wide whole rounds, its three
+// 256-wide rounds taking 3.6 us longer than three 224-wide ones).
+constexpr int64_t kSkTwoWayCost = 40;
+
+// Time of one round of CTA-pair tiles of width bn in the same units (a
+// round of 256-wide tiles = 256): measured over four whole rounds, a
+// 224-wide round takes 0.93 and a 192-wide one 0.90 of a 256-wide one (the
+// k-block's cost hardly depends on the tile width).
+int64_t round_cost(int bn) { return bn == 256 ? 256 : bn == 224 ? 238 : bn == 192 ? 232 : bn; }
 
 int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 
@@ -201,16 +235,23 @@ void plan(const bmm_desc_t* d, Planned* P, int sms, bool row_loader, bool allow_
     else if (!P->pair)
       bn = balanced_tile_n(P->batch, P->Mv, P->Nv, tile_m, u, kMnSingle, 2);
     if (sk_ok) {
-      // Estimated cost in tile-column rounds: whole rounds of the balanced
-      // width, against 256-wide tiles whose leftover round is split along K
-      // (its share of a round plus the fixup; no leftover: no split).
+      // Estimated cost in rounds of 256-wide tiles (x 256): whole rounds of
+      // the balanced width, against 256-wide tiles whose leftover round is
+      // split along K: two ways (the owner's share of a round plus its
+      // fixup) when at most half the pairs hold a leftover tile, else in
+      // equal ranges (the leftover's share of a round plus the fixup).  No
+      // leftover: no split.
       const int64_t tiles_b = P->batch * ((P->Mv + tile_m - 1) / tile_m) * ((P->Nv + bn - 1) / bn);
-      const int64_t cost_b = (tiles_b + u - 1) / u * bn;
+      const int64_t cost_b = (tiles_b + u - 1) / u * round_cost(bn);
       const int64_t tiles_s = P->batch * ((P->Mv + tile_m - 1) / tile_m) * ((P->Nv + 255) / 256);
-      const int64_t cost_s = tiles_s % u == 0 ? tiles_s / u * 256 : tiles_s * 256 / u + kSkFixupCost;
+      const int64_t rem = tiles_s % u;
+      const int64_t owner = k_blocks - sk_contributor_kblocks(k_blocks);
+      const int64_t cost_s = rem == 0       ? tiles_s / u * 256
+                             : 2 * rem <= u ? tiles_s / u * 256 + owner * 256 / k_blocks + kSkTwoWayCost
+                                            : tiles_s * 256 / u + kSkFixupCost;
       if (sk_mode == 2 || cost_s < cost_b) {
         bn = 256;
-        P->sk = tiles_s % u != 0 ? 1 : 0;
+        P->sk = rem != 0 ? 1 : 0;
       }
     }
   }
@@ -270,6 +311,24 @@ void plan(const bmm_desc_t* d, Planned* P, int sms, bool row_loader, bool allow_
   }
   P->stages = stages;
   P->smem_bytes = fixed + static_cast<int64_t>(stages) * P->stage_bytes;
+  // CTA pairs whose C may go out as bf16 through TMA box stores: those
+  // launches need only half the epilogue region, and the ring takes what it
+  // frees (256 x 224 and 256 x 192 tiles: one more stage).  This layout
+  // counts on the dynamic region starting 1024-byte aligned; the kernel
+  // checks that and reports an error (no access) if it does not.
+  P->stages_bf16_box = stages;
+  if (P->pair && d->typeC == BMM_BF16 && !P->swap) {
+    int deep = static_cast<int>((dmt::kSmemLimit - dmt::kEpiBytesBf16 - dmt::kBarBytes) / P->stage_bytes);
+    if (deep > dmt::kMaxStages) deep = dmt::kMaxStages;
+    if (se && *se) {
+      const int cap = std::atoi(se);
+      if (cap >= 2 && cap < deep) deep = cap;
+    }
+    if (deep > stages) {
+      P->stages_bf16_box = deep;
+      P->smem_bytes = dmt::kSmemLimit;
+    }
+  }
 
   uint32_t cols = 32;
   while (cols < static_cast<uint32_t>(2 * bn)) cols <<= 1;
@@ -298,6 +357,7 @@ void fill_info(const Planned& P, const bmm_desc_t* d, bmm_plan_info_t* info) {
   info->tile_n = P.bn;
   info->tile_k = dmt::kTileK;
   info->stages = P.stages;
+  info->stages_bf16_box = P.stages_bf16_box;
   info->swap_ab = P.swap;
   info->pack_a = P.swap ? P.b.pack : P.a.pack;
   info->pack_b = P.swap ? P.a.pack : P.b.pack;
@@ -344,12 +404,12 @@ bool prepare_kernel(int64_t smem) {
   return ok;
 }
 
-template <int BN, bool kSK = false>
+template <int BN, int kTail = 0>
 bool prepare_pair_kernel() {
   static std::once_flag once;
   static bool ok = false;
   std::call_once(once, [] {
-    ok = cudaFuncSetAttribute(dmt::bmm_tc2_kernel<BN, kSK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    ok = cudaFuncSetAttribute(dmt::bmm_tc2_kernel<BN, kTail>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               static_cast<int>(dmt::kSmemLimit)) == cudaSuccess;
   });
   return ok;
@@ -439,16 +499,27 @@ cudaError_t launch_gemm_pair(bmm_plan_s* pl, KParams kp, cudaStream_t stream) {
   }
   int64_t pairs = pl->P.tiles < pl->max_pairs ? pl->P.tiles : pl->max_pairs;
   // Stream-K tail: whole rounds over all resident pairs, then the leftover
-  // tiles' k-blocks in equal ranges (at least kSkMinUnits each) over as many
-  // pairs as that allows.
+  // tiles' k-blocks.  At most half as many leftover tiles as pairs: each tile
+  // on two pairs, the owner's range longer by the partial's transfer time
+  // (sk_piece2).  More: equal ranges (at least kSkMinUnits each) over as many
+  // pairs as that allows (sk_piece).
   const int64_t G = pl->max_pairs;
-  if (BN == 256 && pl->P.sk && pl->sk_ws && G <= kSkFlagBytes / 32 &&
+  bool two_way = false;
+  // (the fixup and a last piece's partial use a quarter of the operand ring:
+  // it must hold a tile row's partial, BN / 32 chunks of 4 KB, and a barrier)
+  const bool ring_ok = static_cast<int64_t>(pl->P.stages) * pl->P.stage_bytes / 4 >= (BN / 32) * 4096 + 128;
+  if (BN == 256 && pl->P.sk && pl->sk_ws && ring_ok && G <= kSkFlagBytes / 32 &&
       sk_workspace_bytes(G, BN) <= pl->P.sk_bytes) {
     const int64_t waves = pl->P.tiles / G, rem = pl->P.tiles % G;
     if (rem > 0) {
       const int64_t units = rem * pl->P.k_blocks;
       int64_t skp = units / sk_min_units(pl->P.k_blocks);
       skp = skp < 1 ? 1 : (skp > G ? G : skp);
+      if (2 * rem <= G) {
+        two_way = true;
+        skp = 2 * rem;
+        kp.sk_ko = pl->P.k_blocks - sk_contributor_kblocks(pl->P.k_blocks);
+      }
       if (++pl->sk_epoch == 0) pl->sk_epoch = 1;
       kp.sk_tiles = static_cast<int32_t>(rem);
       kp.sk_pairs = static_cast<int32_t>(skp);
@@ -460,10 +531,17 @@ cudaError_t launch_gemm_pair(bmm_plan_s* pl, KParams kp, cudaStream_t stream) {
     }
   }
   if constexpr (BN == 256) {
-    if (kp.sk_tiles > 0) {
-      if (!prepare_pair_kernel<BN, true>()) return cudaErrorInvalidValue;
+    if (kp.sk_tiles > 0 && two_way) {
+      if (!prepare_pair_kernel<BN, dmt::kSkTwoWay>()) return cudaErrorInvalidValue;
       cudaLaunchConfig_t cfg = pair_config(pairs, pl->P.smem_bytes, stream, attr, block_threads(kp));
-      return cudaLaunchKernelEx(&cfg, dmt::bmm_tc2_kernel<BN, true>, kp, pl->map[0], pl->map[1], pl->map[2]);
+      return cudaLaunchKernelEx(&cfg, dmt::bmm_tc2_kernel<BN, dmt::kSkTwoWay>, kp, pl->map[0], pl->map[1],
+                                pl->map[2]);
+    }
+    if (kp.sk_tiles > 0) {
+      if (!prepare_pair_kernel<BN, dmt::kSkEven>()) return cudaErrorInvalidValue;
+      cudaLaunchConfig_t cfg = pair_config(pairs, pl->P.smem_bytes, stream, attr, block_threads(kp));
+      return cudaLaunchKernelEx(&cfg, dmt::bmm_tc2_kernel<BN, dmt::kSkEven>, kp, pl->map[0], pl->map[1],
+                                pl->map[2]);
     }
   }
   cudaLaunchConfig_t cfg = pair_config(pairs, pl->P.smem_bytes, stream, attr, block_threads(kp));
@@ -684,6 +762,15 @@ bmm_status_t bmm_run(bmm_plan_t pl, const void* A, const void* B, void* C, float
       if (!encode_c_map(pl, C, &pl->map[2])) return BMM_ERR_CUDA;
       pl->map_ptr[2] = C;
     }
+  }
+  // the pair kernel's epilogue region: half size (and a deeper ring) when C
+  // goes out as bf16 box stores
+  kp.epi_bytes = dmt::kEpiBytes;
+  kp.box_bytes = dmt::kEpiBoxBytes;
+  if (P.pair && kp.c_tma && kp.c_bf16 && P.stages_bf16_box > P.stages) {
+    kp.stages = P.stages_bf16_box;
+    kp.epi_bytes = dmt::kEpiBytesBf16;
+    kp.box_bytes = dmt::kEpiBoxBytesBf16;
   }
   kp.alpha = alpha;
   kp.beta = beta;

@@ -77,7 +77,15 @@ enum WaitSite : uint32_t {
   kSiteTestStall = 5,
   kSiteSchedule = 6,
   kSiteStreamK = 7,
+  kSiteSmemLayout = 8,  // the launch's shared memory does not hold the ring, epilogue and barriers
 };
+
+// Epilogue region of the CTA-pair kernel for launches whose C goes out as
+// bf16 through TMA box stores: two 2 KB boxes (32 rows x 64 bytes) per
+// epilogue warp, half the general region, which leaves room for one more
+// ring stage of 256 x 224 or 256 x 192 tiles.
+constexpr uint32_t kEpiBoxBytesBf16 = 2048u;
+constexpr uint32_t kEpiBytesBf16 = 4u * 2u * kEpiBoxBytesBf16;
 
 // Stream-K tail of the CTA-pair kernel: a piece of k-blocks [ka, kb) of one
 // tile has at least this many k-blocks, and at least half the tile's (so a
@@ -142,8 +150,13 @@ struct KParams {
   int32_t sk_tiles, sk_pairs;
   int64_t sk_first;        // first tile of the tail (whole rounds x pairs)
   uint32_t sk_epoch;       // this launch's flag value (never 0)
+  int32_t sk_ko;           // two-way split: the owner's k-blocks [0, sk_ko), the contributor's the rest
   float4* sk_ws;           // [pair][rank][quarter][chunk][8][32 rows] float4
   uint32_t* sk_flags;      // [pair][rank][quarter]
+  // CTA-pair kernel: bytes of the epilogue region after the ring and of one
+  // box buffer in it (kEpiBytes and kEpiBoxBytes, or for bf16 box-store
+  // launches kEpiBytesBf16 and kEpiBoxBytesBf16)
+  uint32_t epi_bytes, box_bytes;
 };
 
 // A stream-K piece: k-blocks [ka, kb) of tile `tile`.  kind 0: the whole
@@ -193,6 +206,30 @@ __device__ __forceinline__ bool sk_piece(const KParams& p, int64_t pair, int si,
     int64_t q = pair + 1;
     while (q < G && q * U / G < (tt + 1) * KB) ++q;
     it.q_hi = static_cast<int32_t>(q);
+  }
+  return true;
+}
+
+// The two-way split: each of the last sk_tiles tiles runs on two pairs,
+// k-blocks [0, sk_ko) on pair 2i (the owner, which adds the other's partial
+// and writes C) and [sk_ko, k_blocks) on pair 2i+1.  The owner's range is the
+// longer one, by about the time a partial takes to reach the workspace, so
+// the contributor's partial is there when the owner's accumulator is done.
+// At most one piece per pair; false: none.
+__device__ __forceinline__ bool sk_piece2(const KParams& p, int64_t pair, SkPiece& it) {
+  if (pair >= 2 * static_cast<int64_t>(p.sk_tiles)) return false;
+  it.tile = p.sk_first + pair / 2;
+  if ((pair & 1) == 0) {
+    it.ka = 0;
+    it.kb = p.sk_ko;
+    it.kind = 2;
+    it.q_lo = static_cast<int32_t>(pair + 1);
+    it.q_hi = static_cast<int32_t>(pair + 2);
+  } else {
+    it.ka = p.sk_ko;
+    it.kb = p.k_blocks;
+    it.kind = 1;
+    it.q_lo = it.q_hi = 0;
   }
   return true;
 }
@@ -1064,34 +1101,39 @@ __global__ void __launch_bounds__(kThreads, 1)
 // last item and all its MMAs are complete), so the partials come in by bulk
 // copies into `region` (this warp's quarter of the ring: an mbarrier, then
 // 4 KB buffers), as many chunks per batch as the buffers hold.
+// Warp-wide bounded wait (acquire) for a contributor's flag to reach this
+// launch's epoch.  False: the time limit passed (reported) or another role
+// aborted.
+__device__ __forceinline__ bool sk_wait_flag(const KParams& p, const uint32_t* f, int lane, Abort ab) {
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t spin = 0;; ++spin) {
+    if (__all_sync(0xffffffffu, ld_acquire_gpu(f) == p.sk_epoch)) return true;
+    if ((spin & 15u) == 15u) {
+      int bad = 0;
+      if (lane == 0) bad = *ab.flag ? 1 : (global_timer_ns() - t0 > ab.timeout_ns ? 2 : 0);
+      bad = __shfl_sync(0xffffffffu, bad, 0);
+      if (bad) {
+        if (bad == 2 && lane == 0) {
+          *ab.flag = 1u;
+          atomicCAS(ab.err, 0u, kErrTag | (kSiteStreamK << 8) | (blockIdx.x & 0xFFu));
+        }
+        return false;
+      }
+    }
+  }
+}
+
 template <int BN>
 __device__ __forceinline__ bool sk_fixup(const KParams& p, uint8_t* region, uint32_t region_addr,
                                       uint32_t region_bytes, int64_t slot_base_stride, int64_t slot_off,
                                       int q_lo, int q_hi, uint32_t taddr, int lane, Abort ab) {
   const int n = q_hi - q_lo;
   // the contributors' flags: partial written (bounded wait, acquire)
-  for (int x = q_lo; x < q_hi; ++x) {
-    const uint32_t* f = p.sk_flags + (x * slot_base_stride + slot_off) / (BN / 32);
-    const uint64_t t0 = global_timer_ns();
-    for (uint32_t spin = 0;; ++spin) {
-      if (__all_sync(0xffffffffu, ld_acquire_gpu(f) == p.sk_epoch)) break;
-      if ((spin & 15u) == 15u) {
-        int bad = 0;
-        if (lane == 0) bad = *ab.flag ? 1 : (global_timer_ns() - t0 > ab.timeout_ns ? 2 : 0);
-        bad = __shfl_sync(0xffffffffu, bad, 0);
-        if (bad) {
-          if (bad == 2 && lane == 0) {
-            *ab.flag = 1u;
-            atomicCAS(ab.err, 0u, kErrTag | (kSiteStreamK << 8) | (blockIdx.x & 0xFFu));
-          }
-          return false;
-        }
-      }
-    }
-  }
+  for (int x = q_lo; x < q_hi; ++x)
+    if (!sk_wait_flag(p, p.sk_flags + (x * slot_base_stride + slot_off) / (BN / 32), lane, ab)) return false;
   const uint32_t bar = region_addr;
   const uint32_t nbuf = (region_bytes - 128u) / 4096u;
-  const int per_batch = static_cast<int>(nbuf) / n;  // chunks per batch (n <= 2: at least 5)
+  const int per_batch = static_cast<int>(nbuf) / n;  // chunks per batch (n <= 2: at least 4)
   if (lane == 0) {
     mbar_init(bar, 1);
     fence_barrier_init();
@@ -1100,12 +1142,14 @@ __device__ __forceinline__ bool sk_fixup(const KParams& p, uint8_t* region, uint
   uint32_t phase = 0;
   for (int c0 = 0; c0 < BN / 32; c0 += per_batch) {
     const int c1 = c0 + per_batch < BN / 32 ? c0 + per_batch : BN / 32;
+    // contributor x's chunks c0 .. c1-1 are contiguous in its slot: one copy
+    // each, into consecutive buffers
     if (lane == 0) {
       mbar_arrive_expect_tx(bar, static_cast<uint32_t>((c1 - c0) * n) * 4096u);
-      for (int c = c0; c < c1; ++c)
-        for (int x = q_lo; x < q_hi; ++x)
-          bulk_load(region_addr + 128u + static_cast<uint32_t>((c - c0) * n + (x - q_lo)) * 4096u,
-                    p.sk_ws + (x * slot_base_stride + slot_off + c) * 256, 4096u, bar);
+      for (int x = q_lo; x < q_hi; ++x)
+        bulk_load(region_addr + 128u + static_cast<uint32_t>((x - q_lo) * (c1 - c0)) * 4096u,
+                  p.sk_ws + (x * slot_base_stride + slot_off + c0) * 256, static_cast<uint32_t>(c1 - c0) * 4096u,
+                  bar);
     }
     if (!warp_wait_bounded(bar, phase, ab, kSiteStreamK, lane)) return false;
     phase ^= 1u;
@@ -1114,7 +1158,7 @@ __device__ __forceinline__ bool sk_fixup(const KParams& p, uint8_t* region, uint
       tmem_ld_32cols(taddr + 32u * c, v);
       tmem_wait_ld();
       for (int x = 0; x < n; ++x) {
-        const float4* src = reinterpret_cast<const float4*>(region + 128u + ((c - c0) * n + x) * 4096u) + lane;
+        const float4* src = reinterpret_cast<const float4*>(region + 128u + (x * (c1 - c0) + (c - c0)) * 4096u) + lane;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const float4 s4 = src[j * 32];
@@ -1138,15 +1182,40 @@ __device__ __forceinline__ bool sk_fixup(const KParams& p, uint8_t* region, uint
   return true;
 }
 
-// Stream-K piece without its tile's first k-block (kind 1): this warp's 32
-// accumulator rows go to its workspace slot `dst` instead of C (rows as
-// lanes, 8 float4 per row, so each float4 index is a contiguous 512-byte run
-// across the warp), the accumulator is released to the leader (`acce`), and
-// once every lane's stores are visible the flag is raised to this launch's
-// epoch (release).
+// The owner's side of the two-way split: wait for contributor x's flag, bring
+// its partial rows (BN / 32 chunks of 4 KB, contiguous in the slot) into
+// this warp's quarter of the idle operand ring (`region`, past a 128-byte
+// barrier) with one bulk copy, and clear the flag.  The epilogue then adds
+// chunk c (float4 j of lane r at region + 128 + c * 4096 + (j * 32 + r) * 16)
+// to the accumulator's columns as it stores them.
 template <int BN>
-__device__ __forceinline__ void sk_keep_partial(const KParams& p, float4* dst, uint32_t* flag, uint32_t taddr,
-                                             uint32_t acce, int lane) {
+__device__ __forceinline__ bool sk_fetch_partial(const KParams& p, uint32_t region_addr, int64_t slot_base_stride,
+                                              int64_t slot_off, int x, int lane, Abort ab) {
+  uint32_t* f = p.sk_flags + (x * slot_base_stride + slot_off) / (BN / 32);
+  if (!sk_wait_flag(p, f, lane, ab)) return false;
+  const uint32_t bar = region_addr;
+  if (lane == 0) {
+    mbar_init(bar, 1);
+    fence_barrier_init();
+    mbar_arrive_expect_tx(bar, static_cast<uint32_t>(BN / 32) * 4096u);
+    bulk_load(region_addr + 128u, p.sk_ws + (x * slot_base_stride + slot_off) * 256,
+              static_cast<uint32_t>(BN / 32) * 4096u, bar);
+  }
+  __syncwarp();
+  if (!warp_wait_bounded(bar, 0u, ab, kSiteStreamK, lane)) return false;
+  if (lane == 0) *f = 0u;  // consumed: cleared for the next launch
+  return true;
+}
+
+// sk_keep_partial for a piece that is its pair's last item: the operand ring
+// is idle once its accumulator is complete, so the warp lays out all its
+// chunks in its quarter of the ring (`region`, past 128 bytes) and sends the
+// whole partial (BN / 32 chunks of 4 KB, contiguous in the slot) by one bulk
+// copy, then raises the flag.
+template <int BN>
+__device__ __forceinline__ void sk_keep_partial_ring(const KParams& p, float4* dst, uint32_t* flag,
+                                                  uint32_t taddr, uint32_t acce, uint8_t* region,
+                                                  uint32_t region_addr, int lane) {
 #pragma unroll 1
   for (int c = 0; c < BN / 32; ++c) {
     float v[32];
@@ -1157,13 +1226,66 @@ __device__ __forceinline__ void sk_keep_partial(const KParams& p, float4* dst, u
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(acce);
     }
-    float4* d = dst + c * 256 + lane;
+    float4* sb = reinterpret_cast<float4*>(region + 128u + c * 4096u) + lane;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) d[j * 32] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+    for (int j = 0; j < 8; ++j) sb[j * 32] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
   }
-  __threadfence();
+  fence_proxy_async_shared();
   __syncwarp();
-  if (lane == 0) st_release_gpu(flag, p.sk_epoch);
+  if (lane == 0) {
+    bulk_store(dst, region_addr + 128u, static_cast<uint32_t>(BN / 32) * 4096u);
+    bulk_commit_group();
+    bulk_wait_group_all();       // the partial is written
+    fence_proxy_async_global();  // ... and ordered before the flag
+    __threadfence();
+    st_release_gpu(flag, p.sk_epoch);
+  }
+  __syncwarp();
+}
+
+// Stream-K piece without its tile's first k-block (kind 1): this warp's 32
+// accumulator rows go to its workspace slot `dst` instead of C, 4 KB per
+// 32-column chunk (rows as lanes, 8 float4 per row: float4 j of lane r at
+// j * 32 + r).  Each chunk is laid out in one of the warp's two box buffers
+// and sent by one bulk copy (plain stores from the warp would queue in the
+// SM's load/store path); the accumulator is released to the leader
+// (`acce`), and once the copies have completed the flag is raised to this
+// launch's epoch (release).  `nbox` is the warp's box count, shared with the
+// C box stores so the buffer rotation and the read-waits stay in step.
+template <int BN>
+__device__ __forceinline__ void sk_keep_partial(const KParams& p, float4* dst, uint32_t* flag, uint32_t taddr,
+                                             uint32_t acce, uint8_t* boxes, uint32_t boxes_addr,
+                                             uint32_t& nbox, int lane) {
+#pragma unroll 1
+  for (int c = 0; c < BN / 32; ++c) {
+    float v[32];
+    tmem_ld_32cols(taddr + 32u * c, v);
+    tmem_wait_ld();
+    if (c == BN / 32 - 1) {
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(acce);
+    }
+    const uint32_t k = nbox++ & 1u;
+    if (lane == 0) bulk_wait_group_read<1>();  // this buffer's previous copy has been read
+    __syncwarp();
+    float4* sb = reinterpret_cast<float4*>(boxes + k * kEpiBoxBytes) + lane;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) sb[j * 32] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+    fence_proxy_async_shared();
+    __syncwarp();
+    if (lane == 0) {
+      bulk_store(dst + c * 256, boxes_addr + k * kEpiBoxBytes, kEpiBoxBytes);
+      bulk_commit_group();
+    }
+  }
+  if (lane == 0) {
+    bulk_wait_group_all();       // the partial is written
+    fence_proxy_async_global();  // ... and ordered before the flag
+    __threadfence();
+    st_release_gpu(flag, p.sk_epoch);
+  }
+  __syncwarp();
 }
 
 // bmm_tc2_kernel: the same pipeline over CTA pairs (a cluster of 2).  The
@@ -1182,14 +1304,21 @@ __device__ __forceinline__ void sk_keep_partial(const KParams& p, float4* dst, u
 //     empty" barrier (8 arrivals per phase).
 //   - A cluster barrier at the end keeps either CTA from exiting (or freeing
 //     Tensor Memory) while the other can still signal it.
-//   - kSK (stream-K tail, p.sk_tiles > 0): after its whole tiles each pair
-//     runs at most two pieces (sk_piece); see sk_keep_partial and sk_fixup.
-//     A separate instantiation, so launches without a split run code with
-//     none of it.
-template <int BN, bool kSK = false>
+//   - kTail (stream-K tail, p.sk_tiles > 0): after its whole tiles each
+//     pair runs at most two pieces, kSkEven: equal ranges (sk_piece; see
+//     sk_keep_partial and sk_fixup), kSkTwoWay: one piece of a tile split in
+//     two (sk_piece2; the owner adds the partial in its epilogue, see
+//     sk_fetch_partial).  Separate instantiations, so launches without a
+//     split run code with none of it.
+constexpr int kSkEven = 1;
+constexpr int kSkTwoWay = 2;
+
+template <int BN, int kTail = 0>
 __global__ void __launch_bounds__(kThreads, 1)
     bmm_tc2_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmC) {
+  constexpr bool kSK = kTail != 0;
+  constexpr bool kTwo = kTail == kSkTwoWay;
   constexpr int BNH = BN / 2;  // B tile rows held by each CTA
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
@@ -1200,8 +1329,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int S = p.stages;
   const uint32_t ring_bytes = static_cast<uint32_t>(S) * p.stage_bytes;
   float* epi = reinterpret_cast<float*>(smem + ring_bytes);
-  const uint32_t bar0 = sbase + ring_bytes + kEpiBytes;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + ring_bytes + kEpiBytes + 8u * (2u * S + 5u));
+  const uint32_t bar0 = sbase + ring_bytes + p.epi_bytes;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + ring_bytes + p.epi_bytes + 8u * (2u * S + 5u));
   volatile uint32_t* abort_flag = tmem_slot + 1;
 
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
@@ -1210,6 +1339,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto acce_bar = [&](int a) { return bar0 + 8u * (2 * S + 2 + a); };
   const uint32_t drain_bar = bar0 + 8u * (2 * S + 4);
 
+  // The host sizes the ring to the launch's shared memory assuming the
+  // dynamic region starts 1024-byte aligned (no pad); if it does not, every
+  // CTA of the grid (all see the same base) leaves before touching shared
+  // memory, with the error reported, instead of overrunning the region.
+  if (pad + ring_bytes + p.epi_bytes + kBarBytes > dynamic_smem_size()) {
+    if (threadIdx.x == 0) atomicCAS(p.err, 0u, kErrTag | (kSiteSmemLayout << 8) | (blockIdx.x & 0xFFu));
+    return;
+  }
+
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
@@ -1217,6 +1355,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
   // whole tiles, round-robin over the pairs; then (stream-K) at most two pieces
   const int64_t dp_end = kSK ? p.sk_first : p.tiles;
+  auto piece = [&](int si, SkPiece& pc) -> bool {
+    if constexpr (kTwo) return si == 0 && sk_piece2(p, pair, pc);
+    else return sk_piece(p, pair, si, pc);
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -1350,7 +1492,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int64_t t = pair; t < dp_end && ok; t += npairs) load_tile(t, 0, p.k_blocks);
         if constexpr (kSK) {
           SkPiece pc;
-          for (int si = 0; si < 2 && ok && sk_piece(p, pair, si, pc); ++si) load_tile(pc.tile, pc.ka, pc.kb);
+          for (int si = 0; si < 2 && ok && piece(si, pc); ++si) load_tile(pc.tile, pc.ka, pc.kb);
         }
       };
       if constexpr (!kSK) {
@@ -1443,7 +1585,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int64_t t = pair; t < dp_end && ok; t += npairs, ++tl) mma_tile(0, p.k_blocks);
         if constexpr (kSK) {
           SkPiece pc;
-          for (int si = 0; si < 2 && ok && sk_piece(p, pair, si, pc); ++si, ++tl) mma_tile(pc.ka, pc.kb);
+          for (int si = 0; si < 2 && ok && piece(si, pc); ++si, ++tl) mma_tile(pc.ka, pc.kb);
         }
       };
       if constexpr (!kSK) {
@@ -1459,8 +1601,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp < 6) {
     // ------------------------------------------------ epilogue (each CTA)
     const int q = warp & 3;
-    float* stg = epi + (warp - 2) * 32 * kEpiPitch;
-    uint8_t* boxes = reinterpret_cast<uint8_t*>(epi) + (warp - 2) * 2 * kEpiBoxBytes;
+    const uint32_t box_bytes = p.box_bytes;
+    uint8_t* boxes = reinterpret_cast<uint8_t*>(epi) + (warp - 2) * 2 * box_bytes;
+    // the direct-store staging tile: packed after the other warps' tiles, or
+    // (stream-K) inside this warp's own box space, which a piece that keeps
+    // its partial also stages through, so no warp's tile overlaps another's
+    // buffers
+    float* stg = kSK ? reinterpret_cast<float*>(boxes) : epi + (warp - 2) * 32 * kEpiPitch;
     const uint32_t boxes_addr = smem_addr(boxes);
     uint32_t nbox = 0;
     const uint32_t acce_leader0 = mapa_shared(acce_bar(0), 0);
@@ -1481,7 +1628,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (t_next < dp_end) {
         t = t_next;
         t_next += npairs;
-      } else if (kSK && si < 2 && sk_piece(p, pair, si, pc)) {
+      } else if (kSK && si < 2 && piece(si, pc)) {
         ++si;
         t = pc.tile;
         kind = pc.kind;
@@ -1492,10 +1639,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       int b, mb, nb;
       decode_tile(t, p, b, mb, nb);
       const int row0 = mb * (2 * kTileM) + static_cast<int>(rank) * kTileM + q * 32;
+      const int n0 = nb * BN;  // the tile's first column
       const int64_t cbase = static_cast<int64_t>(b) * p.sC;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
       float cin[32];
-      if (pre && kind == 0) prefetch_cin(ea, cin, lane, row0, nb * BN, cbase);
+      if (pre && kind == 0) prefetch_cin(ea, cin, lane, row0, n0, cbase);
       // the epilogue waits a whole mainloop: lane 0 parks (no spinning that
       // would take issue slots from the producer and MMA threads)
       int okw = 1;
@@ -1507,18 +1655,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr int64_t slot_stride = 2 * 4 * (BN / 32);  // float4 blocks of 4 KB per pair
       if (kSK && kind == 1) {
         const int64_t slot_off = (rank * 4 + q) * (BN / 32);
-        sk_keep_partial<BN>(p, p.sk_ws + (pair * slot_stride + slot_off) * 256,
-                            p.sk_flags + (pair * 2 + rank) * 4 + q, taddr,
-                            acc ? acce_leader1 : acce_leader0, lane);
+        float4* dst = p.sk_ws + (pair * slot_stride + slot_off) * 256;
+        uint32_t* flag = p.sk_flags + (pair * 2 + rank) * 4 + q;
+        const uint32_t acce = acc ? acce_leader1 : acce_leader0;
+        SkPiece after;
+        if (!piece(si, after)) {  // the pair's last item: the ring is idle
+          const uint32_t quarter_bytes = ring_bytes / 4u;
+          sk_keep_partial_ring<BN>(p, dst, flag, taddr, acce, smem + (warp - 2) * quarter_bytes,
+                                   sbase + (warp - 2) * quarter_bytes, lane);
+        } else {
+          sk_keep_partial<BN>(p, dst, flag, taddr, acce, boxes, boxes_addr, nbox, lane);
+        }
         continue;
       }
+      // two-way split owner: the contributor's partial rows, added chunk by chunk below
+      const float4* part = nullptr;
       if (kSK && kind == 2) {
         const int64_t slot_off = (rank * 4 + q) * (BN / 32);
         const uint32_t quarter_bytes = ring_bytes / 4u;
-        if (!sk_fixup<BN>(p, smem + (warp - 2) * quarter_bytes, sbase + (warp - 2) * quarter_bytes,
-                          quarter_bytes, slot_stride, slot_off, pc.q_lo, pc.q_hi, taddr, lane, ab))
-          break;
-        if (pre) prefetch_cin(ea, cin, lane, row0, nb * BN, cbase);
+        if constexpr (kTwo) {
+          if (!sk_fetch_partial<BN>(p, sbase + (warp - 2) * quarter_bytes, slot_stride, slot_off, pc.q_lo, lane,
+                                    ab))
+            break;
+          part = reinterpret_cast<const float4*>(smem + (warp - 2) * quarter_bytes + 128u) + lane;
+        } else {
+          if (!sk_fixup<BN>(p, smem + (warp - 2) * quarter_bytes, sbase + (warp - 2) * quarter_bytes,
+                            quarter_bytes, slot_stride, slot_off, pc.q_lo, pc.q_hi, taddr, lane, ab))
+            break;
+        }
+        if (pre) prefetch_cin(ea, cin, lane, row0, n0, cbase);
       }
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
@@ -1530,21 +1695,31 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive_cluster(acc ? acce_leader1 : acce_leader0);
         }
+        if (kTwo && part) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float4 s4 = part[c * 256 + j * 32];
+            v[4 * j] += s4.x;
+            v[4 * j + 1] += s4.y;
+            v[4 * j + 2] += s4.z;
+            v[4 * j + 3] += s4.w;
+          }
+        }
         if (p.c_tma) {
           // skipped outright when wholly outside C (see the single-CTA kernel)
-          if (row0 < p.Mv && nb * BN + 32 * c < p.Nv) {
+          if (row0 < p.Mv && n0 + 32 * c < p.Nv) {
             const uint32_t k = nbox++ & 1u;
-            store_chunk_tma(ea, &tmC, v, boxes + k * kEpiBoxBytes, boxes_addr + k * kEpiBoxBytes, lane,
-                            row0, nb * BN + 32 * c, b);
+            store_chunk_tma(ea, &tmC, v, boxes + k * box_bytes, boxes_addr + k * box_bytes, lane,
+                            row0, n0 + 32 * c, b);
           }
         } else if (pre) {
           float nxt[32];
-          if (c + 1 < BN / 32) prefetch_cin(ea, nxt, lane, row0, nb * BN + 32 * (c + 1), cbase);
-          store_chunk_cin(ea, v, cin, stg, lane, row0, nb * BN + 32 * c, cbase);
+          if (c + 1 < BN / 32) prefetch_cin(ea, nxt, lane, row0, n0 + 32 * (c + 1), cbase);
+          store_chunk_cin(ea, v, cin, stg, lane, row0, n0 + 32 * c, cbase);
 #pragma unroll
           for (int r = 0; r < 32; ++r) cin[r] = nxt[r];
         } else {
-          store_chunk<32>(ea, v, stg, lane, row0, nb * BN + 32 * c, cbase);
+          store_chunk<32>(ea, v, stg, lane, row0, n0 + 32 * c, cbase);
         }
       }
     }

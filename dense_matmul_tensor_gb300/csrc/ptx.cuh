@@ -139,6 +139,22 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       : "memory");
 }
 
+// Untiled bulk copy of `bytes` (a multiple of 16; both addresses 16-byte
+// aligned) from this CTA's shared memory to global, in this thread's current
+// bulk group.
+__device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                   reinterpret_cast<uint64_t>(dst)),
+               "r"(src), "r"(bytes)
+               : "memory");
+}
+
+// Order this thread's completed async-proxy writes to global memory before
+// its later generic-proxy operations (a flag that publishes them).
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 __device__ __forceinline__ void bulk_commit_group() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
@@ -332,6 +348,13 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
 // tcgen05.mma.cta_group::2: each CTA holds its 128 rows of A and half of the
 // B tile in its own shared memory, the even CTA (the leader) issues the MMA,
 // and each CTA's Tensor Memory receives its 128 rows of the accumulator.
+
+// Bytes of dynamic shared memory the launch gave this CTA.
+__device__ __forceinline__ uint32_t dynamic_smem_size() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%dynamic_smem_size;" : "=r"(r));
+  return r;
+}
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;

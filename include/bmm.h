@@ -110,6 +110,11 @@ typedef struct {
                                      pairs are resident (0: none) */
   int64_t sk_workspace_bytes;     /* device memory the plan keeps for the split's fp32
                                      partial sums and flags */
+  int32_t stages_bf16_box;        /* ring depth of runs whose C goes out as bf16 through
+                                     TMA box stores (beta = 0, 16-byte-aligned C): CTA-pair
+                                     plans give those runs half the epilogue buffers and
+                                     the ring the rest; otherwise equal to stages */
+  int32_t reserved0;
 } bmm_plan_info_t;
 
 typedef struct bmm_plan_s* bmm_plan_t;
@@ -162,9 +167,12 @@ BMM_API bmm_status_t bmm_get_plan_info(bmm_plan_t plan, bmm_plan_info_t* info);
  * the row loader; stream_k in bmm_plan_info_t): the CTA pairs first run
  * whole 256 x 256 tiles in rounds; the tiles left over after the last whole
  * round ("Triton Optimization Reference", section 7: the last wave of a
- * persistent grid) are cut along K into equal ranges of k-blocks, one per
- * pair, so every pair finishes at about the same time.  A range covers the
- * end of one tile and the start of the next; the piece of a tile without its
+ * persistent grid) are cut along K.  At most half as many leftover tiles as
+ * resident pairs: each tile runs on two pairs, the one with the first
+ * k-block (the owner) taking a longer range than the other by about the time
+ * the other's partial takes to reach the workspace.  More leftover tiles:
+ * equal ranges of k-blocks, one per pair, a range covering the end of one
+ * tile and the start of the next.  Either way the piece of a tile without its
  * first k-block leaves its fp32 partial sum in the plan's stream-K workspace
  * and raises a flag, and the piece with the first k-block waits for those
  * flags, adds the partials and writes C.  The sum is still accumulated in

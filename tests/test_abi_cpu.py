@@ -128,9 +128,11 @@ def test_planner_on_workloads(lib, name):
     if p is wl.GEMM_4096:
         # CTA pairs with 256 x 224 tiles: 16 x 19 = 304 tiles = exactly 4 rounds
         # on 76 pairs (256-wide tiles would leave a 0.37 wave); 30 KB per CTA
-        # per stage, six stages
+        # per stage, six stages, and seven for the bf16 box-store launches
+        # (7 x 30 KB + 16 KB of boxes + 512 B of barriers = 227 KB - 512 B)
         assert info.cta_pair == 1 and info.tile_n == 224 and info.tiles == 16 * 19
         assert info.stages == 6 and info.tmem_cols == 512
+        assert info.stages_bf16_box == 7 and info.smem_bytes == 232448
         assert info.workspace_bytes == 0
     if p is wl.ATTN_QK:
         # 8192 pair tiles of 256 x 256 fill 108 rounds almost exactly

@@ -36,13 +36,16 @@ def _split_whenever_allowed(monkeypatch):
 
 # (batch, M, N, K, transA, transB): whole rounds plus a tail; only a tail (8
 # tiles on 76 pairs); a ragged K tail inside split pieces; ragged M and N
-# edges; MN-major operands; several batch items.
+# edges; MN-major operands; several batch items.  A leftover of at most half
+# the pairs' tiles is split two ways (sk_piece2), a larger one in equal
+# ranges (sk_piece): 72 tiles on 76 pairs and 74 leftover tiles after a round.
 SHAPES = [
     (1, 4096, 4096, 4096, False, True),
     (1, 512, 1024, 4096, False, True),
     (1, 1000, 1000, 2100, True, False),
     (2, 1100, 700, 3000, False, False),
     (3, 800, 1300, 2048, True, True),
+    (1, 2560, 3840, 2048, False, True),
 ]
 
 
@@ -106,3 +109,15 @@ def test_switched_off_gives_the_same_exact_result(monkeypatch):
     assert info_off.stream_k == 0
     assert np.array_equal(on.view(np.uint32), off.view(np.uint32))
     check_full(p, x, on, exact=True)
+
+
+@pytest.mark.parametrize("publish_kb", ["0", "100"])
+def test_two_way_split_points(monkeypatch, publish_kb):
+    """The owner's range: half the k-blocks (0: no transfer allowance) or all
+    but one (an allowance longer than K)."""
+    monkeypatch.setenv("DMT_BMM_SK_PUBLISH_KB", publish_kb)
+    p = wl.Problem(batch=1, M=1024, N=1536, K=2100, transB=True, type_ab="bf16", type_c="f32", seed=99)
+    x = _ints(p, 991)
+    c, info = run_gpu(p, x)
+    assert info.stream_k == 1 and info.sk_tiles == 24
+    check_full(p, x, c, exact=True)
