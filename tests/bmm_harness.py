@@ -67,21 +67,23 @@ def c_storage(p: wl.Problem, x: wl.Inputs, c_fill: str):
 
 
 def run_gpu(p: wl.Problem, x: wl.Inputs, *, guard=4096, c_fill="nan", stream=None,
-            a_offset=0, expect_status=api.BMM_OK):
+            a_offset=0, c_offset=0, expect_status=api.BMM_OK):
     """Run ``p`` on inputs ``x`` through bmm_create/bmm_run.  Returns
-    (C storage as a host numpy array, plan info)."""
+    (C storage as a host numpy array, plan info).  ``c_offset`` moves C's
+    base that many elements past its 16-byte-aligned place."""
     dev = torch.device("cuda:0")
     A, a0 = _dev16(x.A, guard, NAN_BITS[p.type_ab], dev, a_offset)
     B, b0 = _dev16(x.B, guard, NAN_BITS[p.type_ab], dev)
     chost = c_storage(p, x, c_fill)
+    c0 = guard + c_offset
     if p.type_c == "f32":
-        C = torch.full((guard + chost.size + guard,), float(C_SENTINEL_F32), dtype=torch.float32,
+        C = torch.full((c0 + chost.size + guard,), float(C_SENTINEL_F32), dtype=torch.float32,
                        device=dev)
-        C[guard:guard + chost.size].copy_(torch.from_numpy(chost).to(dev))
+        C[c0:c0 + chost.size].copy_(torch.from_numpy(chost).to(dev))
     else:
-        C = torch.full((guard + chost.size + guard,), _as_i16(C_SENTINEL_BF16), dtype=torch.int16,
+        C = torch.full((c0 + chost.size + guard,), _as_i16(C_SENTINEL_BF16), dtype=torch.int16,
                        device=dev)
-        C[guard:guard + chost.size].copy_(torch.from_numpy(chost.view(np.int16)).to(dev))
+        C[c0:c0 + chost.size].copy_(torch.from_numpy(chost.view(np.int16)).to(dev))
     esz = 2
     cesz = 4 if p.type_c == "f32" else 2
     plan = api.Plan(desc_for(p))
@@ -89,7 +91,7 @@ def run_gpu(p: wl.Problem, x: wl.Inputs, *, guard=4096, c_fill="nan", stream=Non
         info = plan.info()
         st = api.load_library().bmm_run(
             plan.handle, api._ptr(A.data_ptr() + a0 * esz), api._ptr(B.data_ptr() + b0 * esz),
-            api._ptr(C.data_ptr() + guard * cesz), float(p.alpha), float(p.beta),
+            api._ptr(C.data_ptr() + c0 * cesz), float(p.alpha), float(p.beta),
             api._stream(stream if stream is not None else torch.cuda.current_stream()))
         assert st == expect_status, api.bmm_status_string(st)
         torch.cuda.synchronize()
@@ -99,13 +101,13 @@ def run_gpu(p: wl.Problem, x: wl.Inputs, *, guard=4096, c_fill="nan", stream=Non
         plan.close()
     out = C.cpu().numpy()
     if p.type_c == "f32":
-        assert np.all(out[:guard] == C_SENTINEL_F32) and np.all(out[guard + chost.size:] == C_SENTINEL_F32), \
+        assert np.all(out[:c0] == C_SENTINEL_F32) and np.all(out[c0 + chost.size:] == C_SENTINEL_F32), \
             "write outside C"
-        return out[guard:guard + chost.size], info
+        return out[c0:c0 + chost.size], info
     out = out.view(np.uint16)
-    assert np.all(out[:guard] == C_SENTINEL_BF16) and np.all(out[guard + chost.size:] == C_SENTINEL_BF16), \
+    assert np.all(out[:c0] == C_SENTINEL_BF16) and np.all(out[c0 + chost.size:] == C_SENTINEL_BF16), \
         "write outside C"
-    return out[guard:guard + chost.size].copy(), info
+    return out[c0:c0 + chost.size].copy(), info
 
 
 def _batch_slice(p: wl.Problem, x: wl.Inputs, c_host: np.ndarray, b0: int, b1: int):
