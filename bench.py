@@ -60,17 +60,17 @@ RECIPE_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustai
 # keyed by a hash of that kernel's sources and the workload: reported only
 # while those sources are unchanged.
 NCU_TRAFFIC = {
-    ("2fb28f8081b39449", "gemm_4096x4096x4096_tn_bf16"): 86033152 + 17498112,
+    ("d2a3927fed29b42e", "gemm_4096x4096x4096_tn_bf16"): 85172736 + 16939520,
     # captured at batch 64 and scaled by 2 to the batch-128 launch (every query
     # tile does the same work); most of O's write-back happens after the kernel
-    ("4b82bb8108cce335", "attn_fused_b128_2048x2048x128_bf16"): 2 * (100736256 + 6720512),
+    ("f618dee25fb223e6", "attn_fused_b128_2048x2048x128_bf16"): 2 * (100718592 + 5456640),
 }
 # Tensor-pipe activity of the same captures (sm__pipe_tensor_cycles_active,
 # % of elapsed cycles): the hardware's own measure of how busy the tensor
 # cores were, reported beside the fraction of the measured cuBLAS peak.
 NCU_TENSOR_ACTIVE_PCT = {
-    ("2fb28f8081b39449", "gemm_4096x4096x4096_tn_bf16"): 71.56,
-    ("4b82bb8108cce335", "attn_fused_b128_2048x2048x128_bf16"): 40.73,
+    ("d2a3927fed29b42e", "gemm_4096x4096x4096_tn_bf16"): 71.61,
+    ("f618dee25fb223e6", "attn_fused_b128_2048x2048x128_bf16"): 40.87,
 }
 
 # the sources each kernel family is built from
@@ -611,7 +611,10 @@ def main():
                        "transA": p.transA, "transB": p.transB, "inputs": f"{p.type_ab} {p.dist_ab}",
                        "output": p.type_c, "alpha": p.alpha, "beta": p.beta,
                        "l2": f"flushed: {FLUSH_BYTES >> 20} MB write between timed steps",
-                       "tile": [info.tile_m, info.tile_n, info.tile_k], "stages": info.stages,
+                       "tile": [info.tile_m, info.tile_n, info.tile_k],
+                       # ring depth of this launch: pair launches writing bf16 C by box stores take the deeper ring
+                       "stages": (info.stages_bf16_box if (info.cta_pair and p.type_c == "bf16" and p.beta == 0.0)
+                                  else info.stages),
                        "cta_pair": bool(info.cta_pair),
                        "parallelism": f"{world} independent replicas" if world > 1 else "1 GPU"},
             "roofline": roof,

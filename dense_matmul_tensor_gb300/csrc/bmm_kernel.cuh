@@ -1765,9 +1765,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // Copy a strided 16-bit operand into the workspace with ld rounded up to a
 // multiple of 8 elements (16 bytes), which TMA needs for its row strides.
-// Each thread moves one 8-element segment of a row: eight 2-byte loads (the
-// source rows need not be aligned) and one 16-byte store (destination rows
-// are).  Columns past the row end are written as zero; TMA never reads them.
+// Each thread moves one 8-element segment of a row: the one or two aligned
+// 16-byte words that hold it are loaded (the second only when the segment
+// reaches into it, so no load touches a 16-byte word without a byte of the
+// operand: every load stays on a page the operand occupies) and the segment
+// is shifted out of them in registers (source rows need only 2-byte
+// alignment), then stored with one 16-byte store.  Columns past the row end
+// are written as zero; TMA never reads them.
 static __global__ void pack16_kernel(const uint16_t* __restrict__ src, uint16_t* __restrict__ dst,
                               int64_t nb, int64_t rows, int64_t cols, int64_t ld_src,
                               int64_t s_src, int64_t ld_dst, int64_t s_dst) {
@@ -1779,14 +1783,21 @@ static __global__ void pack16_kernel(const uint16_t* __restrict__ src, uint16_t*
     const int64_t b = row / rows, i = row - b * rows;
     const uint16_t* s = src + b * s_src + i * ld_src + seg * 8;
     const int64_t n = (cols - seg * 8) < 8 ? (cols - seg * 8) : 8;
-    uint16_t e[8];
+    const uintptr_t a = reinterpret_cast<uintptr_t>(s);
+    const uint4* w = reinterpret_cast<const uint4*>(a & ~static_cast<uintptr_t>(15));
+    const uint32_t sh = static_cast<uint32_t>(a & 15u);
+    const uint4 lo = __ldg(w);
+    const uint4 hi = sh + 2u * static_cast<uint32_t>(n) > 16u ? __ldg(w + 1) : make_uint4(0u, 0u, 0u, 0u);
+    uint4 q = extract16(lo, hi, sh);
+    if (n < 8) {  // the row's last segment: zero the columns past its end
+      uint32_t e[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-    for (int k = 0; k < 8; ++k) e[k] = k < n ? s[k] : static_cast<uint16_t>(0);
-    uint4 q;
-    q.x = e[0] | (static_cast<uint32_t>(e[1]) << 16);
-    q.y = e[2] | (static_cast<uint32_t>(e[3]) << 16);
-    q.z = e[4] | (static_cast<uint32_t>(e[5]) << 16);
-    q.w = e[6] | (static_cast<uint32_t>(e[7]) << 16);
+      for (int j = 0; j < 4; ++j) {
+        if (2 * j >= n) e[j] = 0u;
+        else if (2 * j + 1 >= n) e[j] &= 0xFFFFu;
+      }
+      q = make_uint4(e[0], e[1], e[2], e[3]);
+    }
     *reinterpret_cast<uint4*>(dst + b * s_dst + i * ld_dst + seg * 8) = q;
   }
 }
