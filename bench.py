@@ -662,6 +662,19 @@ def main():
             del qa, qb, qc
             torch.cuda.empty_cache()
         line["other_workloads"] = other
+        # a GEMM whose tile count is no multiple of the CTA pairs, against the
+        # headline's rate
+        q = wl.UNEVEN_GEMM
+        qa, qb, qc = gpu_inputs(q, dev, 1000 * q.seed)
+        torch.cuda.synchronize()
+        mq, qinfo, _, _ = time_device(q, qa, qb, qc, min(args.steps, 50), 3, flush, stream, lambda: None)
+        mqm = statistics.fmean(mq)
+        tf = q.flops() / (mqm * 1e-3) / 1e12
+        line["uneven_gemm"] = {"workload": q.name, "ms": mqm, "TFLOP/s": tf, "frac_bf16_peak": tf / peaks["bf16_tflops"],
+                               "vs_headline": tf / value, "tile_n": qinfo.tile_n, "tiles": qinfo.tiles,
+                               "stream_k_tiles": qinfo.sk_tiles}
+        del qa, qb, qc
+        torch.cuda.empty_cache()
         pair = {e["workload"]: e["ms"] for e in other}
         qk, pv = wl.ATTN_QK.name, wl.ATTN_PV.name
         pair_ms = pair[qk] + pair[pv] if qk in pair and pv in pair else None

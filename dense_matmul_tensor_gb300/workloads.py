@@ -199,6 +199,12 @@ SKINNY = Problem(batch=1024, M=16, N=256, K=4096, type_ab="bf16", type_c="bf16",
 
 WORKLOADS = {p.name: p for p in (SMALL, GEMM_4096, RAGGED, ATTN_QK, ATTN_PV, SKINNY)}
 
+# A square-GEMM neighbour whose tile count is no multiple of the 76 CTA pairs
+# (16 x 18 = 288 tiles of 256 x 256: 3.79 rounds), measured beside the
+# headline to show how the persistent schedule handles a leftover round.
+UNEVEN_GEMM = Problem(batch=1, M=4000, N=4500, K=4096, transB=True, type_ab="bf16", type_c="bf16",
+                      dist_ab="normal", seed=6, name="gemm_4000x4500x4096_tn_bf16")
+
 
 def attention_qkv(batch=128, L=2048, D=128, Lk=None, seed=None):
     """Q [batch, L, D] and K, V [batch, Lk, D] bit arrays (bf16 normal; Lk = L

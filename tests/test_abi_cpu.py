@@ -194,10 +194,20 @@ def test_stream_k_tail_choice(lib, monkeypatch):
     assert info.stream_k == 1 and info.tile_n == 256 and info.cta_pair == 1
     assert info.tiles == 1024 and info.sk_tiles == 1024 - 13 * 76
     assert info.sk_workspace_bytes >= 76 * 2 * 128 * 256 * 4
-    # 4096^3: four whole rounds of 256 x 224 tiles cost less than 3.37 rounds
-    # of 256 x 256 plus the split's fixup, so no split
+    # 4096^3: four whole rounds of 256 x 224 tiles (0.93 of a 256-wide round
+    # each) cost less than three 256-wide rounds plus the two-way split's
+    # owner range (40 of 64 k-blocks) and fixup, so no split
     g = api.bmm_plan_query(desc_for(wl.GEMM_4096))
     assert g.stream_k == 0 and g.sk_tiles == 0 and g.sk_workspace_bytes == 0 and g.tile_n == 224
+    # 8192^2 x 4096: 36 leftover tiles after 13 rounds, split two ways
+    h = api.bmm_plan_query(_desc(batch=1, M=8192, N=8192, K=4096, lda=4096, ldb=4096, ldc=8192,
+                                 strideA=8192 * 4096, strideB=8192 * 4096, strideC=8192 * 8192, transB=1,
+                                 typeC="bf16"))
+    assert h.stream_k == 1 and h.sk_tiles == 36
+    # 4000 x 4500 x 4096: 288 tiles, 60 leftover after 3 rounds (more than half
+    # the pairs: equal ranges), whose estimate loses to a fourth 256-wide round
+    u = api.bmm_plan_query(desc_for(wl.UNEVEN_GEMM))
+    assert u.stream_k == 0 and u.tile_n == 256 and u.tiles == 288
     # forced on where allowed, off everywhere
     monkeypatch.setenv("DMT_BMM_STREAMK", "1")
     f = api.bmm_plan_query(desc_for(wl.GEMM_4096))

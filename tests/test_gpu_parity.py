@@ -275,6 +275,16 @@ def test_workload_gemm_4096():
     _full_and_seams(p, x, c, info, 1)
 
 
+def test_gemm_with_a_leftover_round():
+    """4000 x 4500 x 4096: 288 pair tiles, no multiple of the 76 pairs (the
+    bench's uneven GEMM), every element against the oracle."""
+    p = wl.UNEVEN_GEMM
+    x = wl.make_inputs(p)
+    c, info = run_gpu(p, x, guard=8192)
+    assert info.cta_pair == 1 and info.tiles % 76 != 0
+    _full_and_seams(p, x, c, info, 6)
+
+
 def test_workload_ragged():
     p = wl.RAGGED
     x = wl.make_inputs(p)
