@@ -287,3 +287,27 @@ def test_host_plan_without_a_gpu_reports_no_device(lib):
     with pytest.raises(api.BmmError) as e:
         api.HostPlan(_desc())
     assert e.value.status == api.BMM_ERR_NO_DEVICE
+
+
+@pytest.mark.parametrize("typeC", ["bf16", "f32"])
+@pytest.mark.parametrize("transB", [0, 1])
+def test_every_ring_layout_fits_the_shared_memory_it_plans(lib, typeC, transB):
+    """For a sweep of shapes: the general layout (1024 bytes of alignment
+    slack, 32 KB of epilogue buffers, 512 bytes of barriers, the ring) fits
+    the plan's shared memory, and a deeper ring for bf16 box-store runs fits
+    the 227 KB limit with 2 KB boxes and no slack (the kernel checks the
+    alignment it counts on at run time)."""
+    stage_limit = 232448
+    for M in (96, 1000, 4096):
+        for N in (16, 100, 333, 999, 4096):
+            for K in (64, 4096):
+                lda, ldb = K, (K if transB else N)
+                d = _desc(batch=1, M=M, N=N, K=K, lda=lda, ldb=ldb, ldc=N, strideA=M * lda,
+                          strideB=(N * K), strideC=M * N, transB=transB, typeC=typeC)
+                i = api.bmm_plan_query(d)
+                assert 2 <= i.stages <= 8
+                assert 1024 + 32768 + 512 + i.stages * i.stage_bytes <= i.smem_bytes <= stage_limit
+                assert i.stages_bf16_box >= i.stages
+                if i.stages_bf16_box > i.stages:
+                    assert i.cta_pair == 1 and typeC == "bf16" and i.swap_ab == 0
+                    assert i.stages_bf16_box * i.stage_bytes + 16384 + 512 <= i.smem_bytes == stage_limit
