@@ -60,17 +60,17 @@ RECIPE_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustai
 # keyed by a hash of that kernel's sources and the workload: reported only
 # while those sources are unchanged.
 NCU_TRAFFIC = {
-    ("d2a3927fed29b42e", "gemm_4096x4096x4096_tn_bf16"): 85172736 + 16939520,
+    ("74de60fa447a3efe", "gemm_4096x4096x4096_tn_bf16"): 86637824 + 17863936,
     # captured at batch 64 and scaled by 2 to the batch-128 launch (every query
     # tile does the same work); most of O's write-back happens after the kernel
-    ("f618dee25fb223e6", "attn_fused_b128_2048x2048x128_bf16"): 2 * (100718592 + 5456640),
+    ("d0000e4da038c4a4", "attn_fused_b128_2048x2048x128_bf16"): 2 * (100719104 + 6902784),
 }
 # Tensor-pipe activity of the same captures (sm__pipe_tensor_cycles_active,
 # % of elapsed cycles): the hardware's own measure of how busy the tensor
 # cores were, reported beside the fraction of the measured cuBLAS peak.
 NCU_TENSOR_ACTIVE_PCT = {
-    ("d2a3927fed29b42e", "gemm_4096x4096x4096_tn_bf16"): 71.61,
-    ("f618dee25fb223e6", "attn_fused_b128_2048x2048x128_bf16"): 40.87,
+    ("74de60fa447a3efe", "gemm_4096x4096x4096_tn_bf16"): 71.44,
+    ("d0000e4da038c4a4", "attn_fused_b128_2048x2048x128_bf16"): 40.76,
 }
 
 # the sources each kernel family is built from

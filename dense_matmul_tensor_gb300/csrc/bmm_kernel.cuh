@@ -709,8 +709,10 @@ __device__ __forceinline__ void store_chunk_tma(const EpiArgs& p, const CUtensor
 // current one and passes each tile index (or the end) to the MMA thread and
 // the epilogue warps through a four-entry ring in shared memory.  A plain
 // launch hands tiles out round-robin over a persistent grid.
-template <int BN, bool kGrouped = false>
-__global__ void __launch_bounds__(kThreads, 1)
+// kPerSM = 2 (grouped launches of narrow tiles): two CTAs of 192 threads
+// share an SM, so the compiler keeps each thread within 168 registers.
+template <int BN, bool kGrouped = false, int kPerSM = 1>
+__global__ void __launch_bounds__(kPerSM == 2 ? kThreads - 32 * kLdgWarps : kThreads, kPerSM)
     bmm_tc_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUtensorMap tmA,
                   const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmC) {
   extern __shared__ uint8_t smem_raw[];
