@@ -100,6 +100,21 @@ def test_grouped_mixed_problems(transA, transB, type_ab, type_c):
         _check(p, x, c)
 
 
+@pytest.mark.parametrize("width", ["256", "128"])
+def test_grouped_pinned_widths(monkeypatch, width):
+    """The default launch runs two CTAs per SM with 128-wide tiles; pinning
+    256 runs one CTA per SM with 256-wide ones.  Problems up to 256 wide, so
+    128-wide tiles split the wider ones in two N tiles."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    monkeypatch.setenv("DMT_BMM_TILE_N", width)
+    probs = _problems(20, 31, False, True, "bf16", "f32")
+    outs, xs, info = _run_group(probs, False, True, "bf16", "f32")
+    assert info["tile_n"] == int(width)
+    for p, x, c in zip(probs, xs, outs):
+        _check(p, x, c)
+
+
 def test_grouped_many_small_problems():
     """A thousand small problems in one launch (the launch-bound case the
     grouping exists for); a sample of them is checked against the oracle."""
