@@ -121,3 +121,20 @@ def test_two_way_split_points(monkeypatch, publish_kb):
     c, info = run_gpu(p, x)
     assert info.stream_k == 1 and info.sk_tiles == 24
     check_full(p, x, c, exact=True)
+
+
+@pytest.mark.parametrize("M,N,K,two_way", [(8192, 8192, 4096, True), (6144, 6144, 4096, False)])
+def test_planner_split_at_full_size(monkeypatch, M, N, K, two_way):
+    """The planner's own choice (no forcing) on shapes where it splits: 8192^2
+    x 4096 (36 leftover tiles, two ways) and 6144^2 x 4096 (44, equal ranges);
+    random bf16 operands, every element against the oracle."""
+    monkeypatch.delenv("DMT_BMM_STREAMK", raising=False)
+    p = wl.Problem(batch=1, M=M, N=N, K=K, transB=True, type_ab="bf16", type_c="bf16", dist_ab="normal", seed=100)
+    info = api.bmm_plan_query(desc_for(p))
+    pairs = 76
+    rem = info.tiles % pairs
+    assert info.stream_k == 1 and info.sk_tiles == rem and (2 * rem <= pairs) == two_way
+    x = wl.make_inputs(p)
+    c, _ = run_gpu(p, x)
+    worst = check_full(p, x, c)
+    print(f"{M}x{N}x{K}: max err/tol over all {M * N} elements = {worst:.4f}")
