@@ -118,6 +118,9 @@ def parse():
     ap.add_argument("--attn-only", type=int, default=None, metavar="BATCH",
                     help="time only the fused attention kernel (L = 2048, D = 128) at this batch "
                          "and print its entry (profiling)")
+    ap.add_argument("--grouped-only", action="store_true",
+                    help="time only the grouped launch of 1000 small problems (no one-call-per-problem "
+                         "comparison) and print its entry (profiling)")
     return ap.parse_args()
 
 
@@ -321,7 +324,7 @@ def time_e2e(p, steps, warmup, stream, dev):
     return ms, h2d, d2h, chunks
 
 
-def grouped_measure(dev, stream, steps, peaks, count=1000, seed=7):
+def grouped_measure(dev, stream, steps, peaks, count=1000, seed=7, compare_singles=True):
     """Many small independent products (M, N, K drawn from 64..256, bf16 in,
     fp32 out): one grouped launch against one bmm_run per problem.  Both
     are timed with CUDA events around the whole set on the same stream (back
@@ -341,8 +344,9 @@ def grouped_measure(dev, stream, steps, peaks, count=1000, seed=7):
         B = torch.randn(K * N, generator=g, device=dev).to(torch.bfloat16)
         C = torch.empty(M * N, dtype=torch.float32, device=dev)
         items.append(dict(M=M, N=N, K=K, lda=K, ldb=N, ldc=N, A=A, B=B, C=C, alpha=1.0, beta=0.0))
-        plans.append(bmm.Plan(bmm.make_desc(batch=1, M=M, N=N, K=K, lda=K, ldb=N, ldc=N, strideA=0,
-                                            strideB=0, strideC=0, typeA="bf16", typeC="f32")))
+        if compare_singles:
+            plans.append(bmm.Plan(bmm.make_desc(batch=1, M=M, N=N, K=K, lda=K, ldb=N, ldc=N, strideA=0,
+                                                strideB=0, strideC=0, typeA="bf16", typeC="f32")))
         flops += 2 * M * N * K
         nbytes += 2 * M * K + 2 * K * N + 4 * M * N
     arr, n = bmm.make_problems(items)
@@ -357,7 +361,8 @@ def grouped_measure(dev, stream, steps, peaks, count=1000, seed=7):
             pl.run(it["A"], it["B"], it["C"], 1.0, 0.0, stream)
 
     out = {}
-    for name, fn in (("grouped", grouped), ("one_call_per_problem", singles)):
+    legs = (("grouped", grouped), ("one_call_per_problem", singles)) if compare_singles else (("grouped", grouped),)
+    for name, fn in legs:
         for _ in range(3):
             fn()
         torch.cuda.synchronize()
@@ -376,8 +381,9 @@ def grouped_measure(dev, stream, steps, peaks, count=1000, seed=7):
         pl.close()
     out.update({"workload": f"grouped_{count}_problems_64_to_256_bf16_f32", "problems": count,
                 "tiles": info["tiles"], "tile_n": info["tile_n"], "algorithmic_bytes": nbytes,
-                "frac_hbm": out["grouped"]["GB/s"] / peaks["hbm_gbs"],
-                "speedup_vs_one_call_per_problem": out["one_call_per_problem"]["ms"] / out["grouped"]["ms"]})
+                "frac_hbm": out["grouped"]["GB/s"] / peaks["hbm_gbs"]})
+    if compare_singles:
+        out["speedup_vs_one_call_per_problem"] = out["one_call_per_problem"]["ms"] / out["grouped"]["ms"]
     return out
 
 
@@ -554,6 +560,12 @@ def main():
         if world > 1:
             dist.barrier()
 
+    if args.grouped_only:
+        peaks_now, _ = load_peaks()
+        entry = grouped_measure(dev, torch.cuda.current_stream(), args.steps, peaks_now, compare_singles=False)
+        if rank == 0:
+            print(json.dumps(entry), flush=True)
+        return
     if args.attn_only is not None:
         flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
         peaks_now, _ = load_peaks()
